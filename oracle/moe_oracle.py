@@ -96,10 +96,11 @@ class ExpertBanks:
     tensors ([n_experts, dim_out, dim_in]).
     """
 
-    def __init__(self, layer: dict, expert_dtype: str):
+    def __init__(self, layer: dict, expert_dtype: str, cache_bytes: int = 3 << 30):
         self.layer = layer
         self.dtype = expert_dtype
         self._cache = {}
+        self._cache_bytes = cache_bytes
 
     def get(self, bank: str, e: int) -> np.ndarray:
         key = (bank, int(e))
@@ -111,8 +112,9 @@ class ExpertBanks:
                                           self.layer[bank + "_min"][e])
             else:
                 m = to_f64(self.layer[bank][e], self.dtype)
-            if len(self._cache) > 96:
-                self._cache.clear()
+            held = sum(v.nbytes for v in self._cache.values())
+            while self._cache and held + m.nbytes > self._cache_bytes:
+                held -= self._cache.pop(next(iter(self._cache))).nbytes
             self._cache[key] = m
         return m
 

@@ -1,0 +1,405 @@
+// C ABI of the MoE layer forward: argument validation, workspace plan and the
+// launch sequence on the caller's stream. See include/moe_route.h.
+#include "moe_route.h"
+
+#include <math.h>
+#include <atomic>
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kTcBm = 128;  // token rows per tensor-core tile
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct Plan {
+  size_t ctrl, logits, s_shared, counts, offsets, active, perm, pos, rowblocks;
+  size_t H, Hs, Y, Ys, total;
+};
+
+Plan make_plan(const moe_cfg_t& c) {
+  Plan p{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  const size_t T = c.T, E = c.n_experts, P = (size_t)c.T * c.top_k;
+  const size_t d = c.d_model, I = c.d_ff, Is = c.d_ff_shared;
+  p.ctrl = take(sizeof(Ctrl));
+  p.logits = take(T * (E + 1) * 4);
+  p.s_shared = take(T * 4);
+  p.counts = take(E * 4);
+  p.offsets = take((E + 1) * 4);
+  p.active = take(E * 4);
+  p.perm = take(P * 4);
+  p.pos = take(P * 4);
+  p.rowblocks = take(((P + T) / kTcBm + E + 2) * 8);
+  p.H = take(P * I * 4);
+  p.Hs = take(T * Is * 4);
+  p.Y = take(P * d * 4);
+  p.Ys = take(Is ? T * d * 4 : 0);
+  p.total = off;
+  return p;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+moe_status_t validate_cfg(const moe_cfg_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d_model <= 0 || (c->d_model % 8) != 0) return MOE_ERR_INVALID_ARG;
+  if (c->n_experts < 1 || c->top_k < 1 || c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
+  if (c->d_ff <= 0 || (c->d_ff % 8) != 0) return MOE_ERR_INVALID_ARG;
+  if (c->d_ff_shared < 0 || (c->d_ff_shared % 8) != 0) return MOE_ERR_INVALID_ARG;
+  if (c->router == MOE_ROUTER_SIGMOID_GROUP_TOPK) {
+    if (c->n_group < 1 || (c->n_experts % c->n_group) != 0) return MOE_ERR_INVALID_ARG;
+    if (c->topk_group < 1 || c->topk_group > c->n_group) return MOE_ERR_INVALID_ARG;
+    if ((long long)c->topk_group * (c->n_experts / c->n_group) < c->top_k)
+      return MOE_ERR_INVALID_ARG;
+    if (c->n_group > 32) return MOE_ERR_UNSUPPORTED;
+  } else if (c->router != MOE_ROUTER_SOFTMAX_TOPK) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!isfinite(c->routed_scaling) || !isfinite(c->renorm_clamp) || c->renorm_clamp < 0.f)
+    return MOE_ERR_INVALID_ARG;
+  if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->expert_dtype != MOE_F32 && c->expert_dtype != MOE_BF16 &&
+      c->expert_dtype != MOE_Q4_AFFINE_G64)
+    return MOE_ERR_INVALID_ARG;
+  if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_TC) return MOE_ERR_INVALID_ARG;
+  // limits of this build
+  if (c->n_experts > 512 || c->top_k > 32) return MOE_ERR_UNSUPPORTED;
+  if (c->expert_dtype == MOE_F32 && c->act_dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
+  if (c->expert_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c->expert_dtype == MOE_Q4_AFFINE_G64) return MOE_ERR_UNSUPPORTED;  // not built yet
+  if (c->path == MOE_PATH_TC) return MOE_ERR_UNSUPPORTED;                // not built yet
+  return MOE_OK;
+}
+
+moe_status_t check_workspace(const moe_cfg_t* c) {
+  if (!c->workspace || ((uintptr_t)c->workspace & 255u)) return MOE_ERR_WORKSPACE;
+  if (c->workspace_bytes < make_plan(*c).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename T>
+T* at(const moe_cfg_t* c, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(c->workspace) + off);
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ---------------------------------------------------------------------------
+// measurement: launch counter and optional event bracketing of one kernel
+// ---------------------------------------------------------------------------
+std::atomic<unsigned long long> g_launches{0};
+struct TraceState {
+  int kernel = 0;
+  cudaEvent_t* starts = nullptr;
+  cudaEvent_t* stops = nullptr;
+  int n = 0;
+  int* count = nullptr;
+} g_trace;
+
+// Runs one kernel launcher, counting it and bracketing it with the traced
+// events when its family is being traced.
+template <typename F>
+cudaError_t run(int kid, cudaStream_t st, F&& launch) {
+  const bool tr = g_trace.kernel == kid && g_trace.n > 0;
+  const int slot = tr ? (*g_trace.count % g_trace.n) : 0;
+  if (tr && cudaEventRecord(g_trace.starts[slot], st) != cudaSuccess) return cudaErrorUnknown;
+  cudaError_t e = launch();
+  if (e != cudaSuccess) return e;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (tr) {
+    if (cudaEventRecord(g_trace.stops[slot], st) != cudaSuccess) return cudaErrorUnknown;
+    ++*g_trace.count;
+  }
+  return cudaSuccess;
+}
+
+bool bank_ok(const moe_bank_t& b, int dt) {
+  if (!b.w || !aligned16(b.w)) return false;
+  if (dt == MOE_Q4_AFFINE_G64) return b.scale && b.minv && aligned16(b.scale) && aligned16(b.minv);
+  return true;
+}
+
+moe_status_t enqueue_route(const void* x, const void* W_router, const float* bias,
+                           const void* w_shared, const moe_cfg_t* c, int32_t* ids, float* w,
+                           float* s_shared, cudaStream_t st) {
+  const Plan p = make_plan(*c);
+  RouterArgs ra{x, W_router, s_shared ? w_shared : nullptr, at<float>(c, p.logits), c->T,
+                c->d_model, c->n_experts};
+  TopkArgs ta{};
+  ta.logits = ra.logits;
+  ta.bias = c->router == MOE_ROUTER_SIGMOID_GROUP_TOPK ? bias : nullptr;
+  ta.topk_ids = ids;
+  ta.weights = w;
+  ta.s_shared = s_shared;
+  ta.T = c->T;
+  ta.E = c->n_experts;
+  ta.k = c->top_k;
+  ta.kind = c->router;
+  ta.n_group = c->n_group;
+  ta.topk_group = c->topk_group;
+  ta.has_shared_logit = ra.w_shared ? 1 : 0;
+  ta.routed_scaling = c->routed_scaling;
+  ta.renorm_clamp = c->renorm_clamp;
+  const bool bf16 = c->act_dtype == MOE_BF16;
+  cudaError_t e = run(MOE_KERNEL_ROUTER_LOGITS, st,
+                      [&] { return launch_router_logits(ra, bf16, st); });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(run(MOE_KERNEL_ROUTER_TOPK, st, [&] { return launch_router_topk(ta, st); }));
+}
+
+moe_status_t enqueue_bucket(const int32_t* ids, const moe_cfg_t* c, int32_t* counts,
+                            int32_t* offsets, int32_t* active, int32_t* n_active, int32_t* perm,
+                            int32_t* pos, cudaStream_t st) {
+  BucketArgs b{};
+  b.ids = ids;
+  b.counts = counts;
+  b.offsets = offsets;
+  b.active = active;
+  b.n_active = n_active;
+  b.perm = perm;
+  b.pos = pos;
+  b.ctrl = at<Ctrl>(c, 0);
+  b.P = c->T * c->top_k;
+  b.E = c->n_experts;
+  b.rowblocks = nullptr;
+  return cuda_status(run(MOE_KERNEL_BUCKET, st, [&] { return launch_bucket(b, st); }));
+}
+
+moe_status_t enqueue_experts(const void* x, const float* r_attn, const float* alpha,
+                             const float* s_shared, moe_bank_t Wg, moe_bank_t Wu, moe_bank_t Wd,
+                             const void* Wsg, const void* Wsu, const void* Wsd,
+                             const moe_cfg_t* c, float* out, cudaStream_t st) {
+  const Plan p = make_plan(*c);
+  Ctrl* ctrl = at<Ctrl>(c, 0);
+  GemvArgs g{};
+  g.x = x;
+  g.perm = at<int32_t>(c, p.perm);
+  g.active = at<int32_t>(c, p.active);
+  g.offsets = at<int32_t>(c, p.offsets);
+  g.n_active = &ctrl->n_active;
+  g.alpha = alpha;
+  g.s_shared = s_shared;
+  g.Wg = Wg.w; g.Wu = Wu.w; g.Wd = Wd.w;
+  g.Wg_scale = Wg.scale; g.Wg_min = Wg.minv;
+  g.Wu_scale = Wu.scale; g.Wu_min = Wu.minv;
+  g.Wd_scale = Wd.scale; g.Wd_min = Wd.minv;
+  g.Wsg = Wsg; g.Wsu = Wsu; g.Wsd = Wsd;
+  g.H = at<float>(c, p.H);
+  g.Hs = at<float>(c, p.Hs);
+  g.Y = at<float>(c, p.Y);
+  g.Ys = at<float>(c, p.Ys);
+  g.ctrl = ctrl;
+  g.T = c->T; g.d = c->d_model; g.E = c->n_experts; g.k = c->top_k;
+  g.I = c->d_ff; g.Is = c->d_ff_shared; g.P = c->T * c->top_k;
+  g.routed_slots = g.P < g.E ? g.P : g.E;
+  g.has_shared = c->d_ff_shared > 0 ? 1 : 0;
+  const int act = c->act_dtype == MOE_BF16 ? 1 : 0;
+  const int wdt = c->expert_dtype == MOE_F32 ? 0 : (c->expert_dtype == MOE_BF16 ? 1 : 2);
+  cudaError_t e = run(MOE_KERNEL_GEMV_GATEUP, st,
+                      [&] { return launch_gemv_gateup(g, act, wdt, st); });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = run(MOE_KERNEL_GEMV_DOWN, st, [&] { return launch_gemv_down(g, act, wdt, st); });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  CombineArgs cb{r_attn, g.Y, g.has_shared ? g.Ys : nullptr, at<int32_t>(c, p.pos), out,
+                 c->T, c->d_model, c->top_k};
+  return cuda_status(run(MOE_KERNEL_COMBINE, st, [&] { return launch_combine(cb, st); }));
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ROUTE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: outside this build's limits";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace null, too small or misaligned";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or launch failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+    case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK: a device-side check failed";
+  }
+  return "unknown moe_status_t";
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status_t moe_trace_kernel(int kernel, void* const* starts, void* const* stops, int n,
+                              int* count) {
+  if (kernel == 0) {
+    g_trace = TraceState{};
+    return MOE_OK;
+  }
+  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_TC_DOWN || n <= 0 || !starts ||
+      !stops || !count)
+    return MOE_ERR_INVALID_ARG;
+  g_trace.kernel = kernel;
+  g_trace.starts = (cudaEvent_t*)starts;
+  g_trace.stops = (cudaEvent_t*)stops;
+  g_trace.n = n;
+  g_trace.count = count;
+  *count = 0;
+  return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_cfg_t* cfg) {
+  moe_status_t s = validate_cfg(cfg);
+  if (s != MOE_OK && s != MOE_ERR_UNSUPPORTED) return 0;
+  return make_plan(*cfg).total;
+}
+
+moe_status_t moe_workspace_init(const moe_cfg_t* cfg, void* stream) {
+  if (!cfg || !cfg->workspace || ((uintptr_t)cfg->workspace & 255u) ||
+      cfg->workspace_bytes < sizeof(Ctrl))
+    return MOE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(cfg->workspace, 0, sizeof(Ctrl), (cudaStream_t)stream));
+}
+
+moe_status_t moe_read_device_status(const moe_cfg_t* cfg, void* stream, uint32_t* info) {
+  if (!cfg || !cfg->workspace || cfg->workspace_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t word = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(&word, cfg->workspace, sizeof(word), cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(cfg->workspace, 0, sizeof(word), st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (info) *info = word;
+  if (word & kDevTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+  if (word & 0xFFFFu) return MOE_ERR_DEVICE_CHECK;
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const void* x, const void* W_router, const float* expert_bias,
+                       const void* w_shared, const moe_cfg_t* cfg, int32_t* topk_ids,
+                       float* weights, float* s_shared, void* stream) {
+  moe_status_t s = validate_cfg(cfg);
+  if (s != MOE_OK && s != MOE_ERR_UNSUPPORTED) return s;
+  if (cfg->n_experts > 512 || cfg->top_k > 32 || cfg->n_group > 32) return MOE_ERR_UNSUPPORTED;
+  if ((s = check_workspace(cfg)) != MOE_OK) return s;
+  if (cfg->T == 0) return MOE_OK;
+  if (!x || !W_router || !topk_ids || !weights) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_router) || !aligned16(topk_ids) || !aligned16(weights))
+    return MOE_ERR_INVALID_ARG;
+  if (s_shared && (!w_shared || !aligned16(w_shared) || !aligned16(s_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if (expert_bias && !aligned16(expert_bias)) return MOE_ERR_INVALID_ARG;
+  return enqueue_route(x, W_router, expert_bias, w_shared, cfg, topk_ids, weights, s_shared,
+                       (cudaStream_t)stream);
+}
+
+moe_status_t moe_bucket(const int32_t* topk_ids, const moe_cfg_t* cfg, int32_t* counts,
+                        int32_t* offsets, int32_t* active, int32_t* n_active, int32_t* perm,
+                        int32_t* pos, void* stream) {
+  moe_status_t s = validate_cfg(cfg);
+  if (s != MOE_OK && s != MOE_ERR_UNSUPPORTED) return s;
+  if (cfg->n_experts > 512) return MOE_ERR_UNSUPPORTED;
+  if ((s = check_workspace(cfg)) != MOE_OK) return s;
+  if (cfg->T == 0) return MOE_OK;
+  const void* ptrs[] = {topk_ids, counts, offsets, active, n_active, perm, pos};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  return enqueue_bucket(topk_ids, cfg, counts, offsets, active, n_active, perm, pos,
+                        (cudaStream_t)stream);
+}
+
+moe_status_t moe_experts_forward(const void* x, const float* r_attn, const int32_t* topk_ids,
+                                 const float* weights, const float* s_shared, moe_bank_t W_gate,
+                                 moe_bank_t W_up, moe_bank_t W_down, const void* Ws_gate,
+                                 const void* Ws_up, const void* Ws_down, const void* w_shared,
+                                 const moe_cfg_t* cfg, float* out, void* stream) {
+  moe_status_t s = validate_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if ((s = check_workspace(cfg)) != MOE_OK) return s;
+  if (cfg->T == 0) return MOE_OK;
+  const void* ptrs[] = {x, r_attn, topk_ids, weights, out};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (!bank_ok(W_gate, cfg->expert_dtype) || !bank_ok(W_up, cfg->expert_dtype) ||
+      !bank_ok(W_down, cfg->expert_dtype))
+    return MOE_ERR_INVALID_ARG;
+  const bool shared = cfg->d_ff_shared > 0;
+  if (shared) {
+    const void* sp[] = {Ws_gate, Ws_up, Ws_down};
+    for (const void* q : sp)
+      if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    if (!s_shared && !w_shared) return MOE_ERR_INVALID_ARG;
+    if ((s_shared && !aligned16(s_shared)) || (w_shared && !aligned16(w_shared)))
+      return MOE_ERR_INVALID_ARG;
+  }
+  if ((const void*)out == x) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const Plan p = make_plan(*cfg);
+  if (shared && !s_shared) {
+    // shared gate only: the router with zero routed rows
+    RouterArgs ra{x, nullptr, w_shared, at<float>(cfg, p.logits), cfg->T, cfg->d_model, 0};
+    const bool bf16 = cfg->act_dtype == MOE_BF16;
+    cudaError_t e = run(MOE_KERNEL_SHARED_GATE, st, [&] {
+      return launch_shared_gate(ra, at<float>(cfg, p.s_shared), bf16, st);
+    });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    s_shared = at<float>(cfg, p.s_shared);
+  }
+  s = enqueue_bucket(topk_ids, cfg, at<int32_t>(cfg, p.counts), at<int32_t>(cfg, p.offsets),
+                     at<int32_t>(cfg, p.active), &at<Ctrl>(cfg, 0)->n_active,
+                     at<int32_t>(cfg, p.perm), at<int32_t>(cfg, p.pos), st);
+  if (s != MOE_OK) return s;
+  return enqueue_experts(x, r_attn, weights, s_shared, W_gate, W_up, W_down, Ws_gate, Ws_up,
+                         Ws_down, cfg, out, st);
+}
+
+moe_status_t moe_layer_forward(const void* x, const float* r_attn, const void* W_router,
+                               const float* expert_bias, moe_bank_t W_gate, moe_bank_t W_up,
+                               moe_bank_t W_down, const void* Ws_gate, const void* Ws_up,
+                               const void* Ws_down, const void* w_shared, const moe_cfg_t* cfg,
+                               float* out, int32_t* topk_ids, float* weights, void* stream) {
+  moe_status_t s = validate_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if ((s = check_workspace(cfg)) != MOE_OK) return s;
+  if (cfg->T == 0) return MOE_OK;
+  const void* ptrs[] = {x, r_attn, W_router, out, topk_ids, weights};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (expert_bias && !aligned16(expert_bias)) return MOE_ERR_INVALID_ARG;
+  if (!bank_ok(W_gate, cfg->expert_dtype) || !bank_ok(W_up, cfg->expert_dtype) ||
+      !bank_ok(W_down, cfg->expert_dtype))
+    return MOE_ERR_INVALID_ARG;
+  const bool shared = cfg->d_ff_shared > 0;
+  if (shared) {
+    const void* sp[] = {Ws_gate, Ws_up, Ws_down, w_shared};
+    for (const void* q : sp)
+      if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  }
+  if ((const void*)out == x) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const Plan p = make_plan(*cfg);
+  float* s_sh = shared ? at<float>(cfg, p.s_shared) : nullptr;
+  s = enqueue_route(x, W_router, expert_bias, shared ? w_shared : nullptr, cfg, topk_ids, weights,
+                    s_sh, st);
+  if (s != MOE_OK) return s;
+  s = enqueue_bucket(topk_ids, cfg, at<int32_t>(cfg, p.counts), at<int32_t>(cfg, p.offsets),
+                     at<int32_t>(cfg, p.active), &at<Ctrl>(cfg, 0)->n_active,
+                     at<int32_t>(cfg, p.perm), at<int32_t>(cfg, p.pos), st);
+  if (s != MOE_OK) return s;
+  return enqueue_experts(x, r_attn, weights, s_sh, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
+                         cfg, out, st);
+}
+
+}  // extern "C"

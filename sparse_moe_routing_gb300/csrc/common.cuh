@@ -1,0 +1,101 @@
+// Device-side helpers shared by the MoE layer kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// workspace control block (first 256 bytes of every workspace)
+// ---------------------------------------------------------------------------
+enum : uint32_t {
+  kDevBadId = 1u << 0,     // an expert id outside [0, E) was seen
+  kDevTimeout = 1u << 1,   // a bounded wait gave up
+  kDevBadShape = 1u << 2,  // a device-side shape check failed
+};
+
+// Sites recorded in the upper 16 bits of the status word (first failure wins).
+enum : uint32_t {
+  kSiteBucket = 1,
+  kSiteGemvGateUp = 2,
+  kSiteGemvDown = 3,
+  kSiteCombine = 4,
+  kSiteTcGateUp = 5,
+  kSiteTcDown = 6,
+  kSiteTcRouter = 7,
+  kSiteRouter = 8,
+};
+
+struct Ctrl {
+  uint32_t status;        // error bits (low 16) | first failing site (high 16)
+  int32_t n_active;       // active routed experts (bucket)
+  int32_t n_rowblocks;    // tensor-core path: (group, m-tile) row blocks
+  int32_t pad0;
+  uint32_t arrive[8];     // self-resetting arrival counters
+  int32_t pad[52];
+};
+static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
+
+__device__ __forceinline__ void report(Ctrl* c, uint32_t bits, uint32_t site) {
+  uint32_t old = atomicOr(&c->status, bits);
+  if ((old >> 16) == 0) atomicCAS(&c->status, old | bits, (old | bits) | (site << 16));
+}
+
+// ---------------------------------------------------------------------------
+// element helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 16-byte streaming load that bypasses L1 allocation (weights are read once).
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+// Unpacks a 16-byte chunk of weights into floats. Element type selects the
+// count: 8 bf16 or 4 f32 per chunk.
+template <typename TW> struct Chunk;
+template <> struct Chunk<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* w) {
+    w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x); w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
+    w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z); w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
+  }
+};
+template <> struct Chunk<float> {
+  static constexpr int kVec = 4;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* w) {
+    w[0] = __uint_as_float(v.x); w[1] = __uint_as_float(v.y);
+    w[2] = __uint_as_float(v.z); w[3] = __uint_as_float(v.w);
+  }
+};
+
+__device__ __forceinline__ float load_act(const float* p, size_t i) { return p[i]; }
+__device__ __forceinline__ float load_act(const __nv_bfloat16* p, size_t i) {
+  return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void store_act(float* p, size_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void store_act(__nv_bfloat16* p, size_t i, float v) {
+  p[i] = __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + __expf(-v)); }
+__device__ __forceinline__ float siluf_(float v) { return v / (1.0f + __expf(-v)); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace moe

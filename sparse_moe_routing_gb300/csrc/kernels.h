@@ -1,0 +1,90 @@
+// Kernel argument blocks and launchers of the MoE layer (host + device).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct Ctrl;
+
+struct RouterArgs {
+  const void* x;          // [T][d] act dtype
+  const void* W_router;   // [E][d]
+  const void* w_shared;   // [d] or null (then no column E)
+  float* logits;          // [T][E+1] f32
+  int T, d, E;
+};
+
+struct TopkArgs {
+  const float* logits;    // [T][E+1]
+  const float* bias;      // [E] or null
+  int32_t* topk_ids;      // [T][k]
+  float* weights;         // [T][k]
+  float* s_shared;        // [T] or null
+  int T, E, k, kind, n_group, topk_group, has_shared_logit;
+  float routed_scaling, renorm_clamp;
+};
+
+struct BucketArgs {
+  const int32_t* ids;     // [P]
+  int32_t* counts;        // [E]
+  int32_t* offsets;       // [E+1]
+  int32_t* active;        // [E]
+  int32_t* n_active;      // [1] (may point into Ctrl)
+  int32_t* perm;          // [P]
+  int32_t* pos;           // [P]
+  Ctrl* ctrl;
+  int P, E;
+  // tensor-core path work list (null when unused): row blocks of bm rows,
+  // one int2 {group, m_tile} each, largest groups first; shared group = E
+  int2* rowblocks;
+  int32_t* n_rowblocks;
+  int bm, shared_rows;    // shared_rows = T when a shared expert exists, else 0
+};
+
+// Grouped GEMV over the packed rows ("groups" = active routed experts, then
+// the shared expert as group E).
+struct GemvArgs {
+  const void* x;            // [T][d] act dtype
+  const int32_t* perm;      // packed row -> pair id
+  const int32_t* active;
+  const int32_t* offsets;   // [E+1]
+  const int32_t* n_active;  // device count
+  const float* alpha;       // [P] flattened routing weights
+  const float* s_shared;    // [T]
+  const void* Wg; const void* Wu; const void* Wd;              // routed banks
+  const void* Wg_scale; const void* Wg_min;                    // q4 only
+  const void* Wu_scale; const void* Wu_min;
+  const void* Wd_scale; const void* Wd_min;
+  const void* Wsg; const void* Wsu; const void* Wsd;           // shared expert
+  float* H;                 // [P][I] f32
+  float* Hs;                // [T][Is] f32
+  float* Y;                 // [P][d] f32 (alpha applied)
+  float* Ys;                // [T][d] f32 (s_shared applied)
+  Ctrl* ctrl;
+  int T, d, E, k, I, Is, P;
+  int routed_slots;         // grid.y entries for routed groups (= min(E, P))
+  int has_shared;
+};
+
+struct CombineArgs {
+  const float* r_attn;      // [T][d]
+  const float* Y;           // [P][d]
+  const float* Ys;          // [T][d] or null
+  const int32_t* pos;       // [P]
+  float* out;               // [T][d]
+  int T, d, k;
+};
+
+// One launcher per kernel; each returns the launch's cudaError_t.
+cudaError_t launch_router_logits(const RouterArgs& ra, bool bf16, cudaStream_t st);
+cudaError_t launch_router_topk(const TopkArgs& ta, cudaStream_t st);
+cudaError_t launch_shared_gate(const RouterArgs& ra, float* s_out, bool bf16, cudaStream_t st);
+cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t st);
+// act: 0 f32, 1 bf16; wdt: 0 f32, 1 bf16, 2 q4
+cudaError_t launch_gemv_gateup(const GemvArgs& a, int act, int wdt, cudaStream_t st);
+cudaError_t launch_gemv_down(const GemvArgs& a, int act, int wdt, cudaStream_t st);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,257 @@
+"""GPU parity of the CUDA path with the fp64 oracle, through the C ABI.
+
+Criteria (stated once here, applied throughout):
+  * routing ids: bit-exact wherever the oracle's gap between the k-th and
+    (k+1)-th ranking score (and for groups, between the topk_group-th and next
+    group score) exceeds 1e-4; near-ties are counted and must be valid choices;
+  * routing weights: within 1e-5 absolute;
+  * bucketing: bit-exact (integers);
+  * layer output: max |out - ref| / rms(ref) <= 2e-2 (bf16) or 1e-4 (fp32).
+Small cases compare every element; full-size cases compare the routing of
+every token and the outputs of a seeded sample of tokens (each output row
+depends only on its own token, so the oracle computes sampled rows exactly).
+"""
+import numpy as np
+import pytest
+
+import moe_inputs as mi
+import oracle as orc
+from gpu_util import (OUT_TOL, DevLayer, cfg_for, check_routing, layer_host, rel_rms_err,
+                      to_dev)
+
+pytestmark = pytest.mark.gpu
+
+import torch  # noqa: E402
+
+import sparse_moe_routing_gb300 as smr  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_moe_routing_gb300 import build
+    build.build()
+    smr.lib()
+
+
+def _oracle_routing(L, shape):
+    x = orc.to_f64(L["x"], shape.act_dtype)
+    W = orc.to_f64(L["W_router"], shape.act_dtype)
+    bias = None if "expert_bias" not in L else L["expert_bias"].astype(np.float64)
+    return orc.route_tokens(orc.router_logits(x, W), shape, bias)
+
+
+def _sample(T, n, seed=0):
+    if T <= n:
+        return np.arange(T)
+    rng = np.random.default_rng(seed)
+    s = np.sort(rng.choice(T, size=n - 2, replace=False))
+    return np.unique(np.concatenate([[0, T - 1], s]))
+
+
+def _run_layer(shape, T, path=smr.PATH_AUTO):
+    L = layer_host(shape, T)
+    dev = DevLayer(shape, L)
+    cfg = cfg_for(shape, T, path)
+    ws = smr.alloc_workspace(cfg)
+    dev.layer_forward(cfg, ws)
+    st, word = smr.read_device_status(cfg, ws)
+    assert st == 0, (st, hex(word))
+    return L, dev, cfg, ws
+
+
+# (shape, T, number of output rows the oracle checks)
+CASES = [
+    (mi.TINY_F32, 32, 32),
+    (mi.TINY_F32.with_(name="tiny_f32_ragged"), 37, 37),
+    (mi.QWEN36, 1, 1),
+    (mi.QWEN36, 8, 8),
+    (mi.QWEN36, 64, 64),
+    (mi.QWEN36, 37, 37),
+    (mi.DEEPSEEK_GROUP, 1, 1),
+    (mi.DEEPSEEK_GROUP, 64, 64),
+    (mi.QWEN36_PREFILL_SKEW, 4096, 24),
+    (mi.DEEPSEEK_GROUP, 4096, 24),
+    (mi.MIXTRAL, 2048, 6),
+]
+
+
+@pytest.mark.parametrize("shape,T,n_check", CASES,
+                         ids=["%s-T%d" % (c[0].name, c[1]) for c in CASES])
+def test_layer_forward_parity(shape, T, n_check):
+    L, dev, cfg, ws = _run_layer(shape, T)
+    gpu_ids = dev.ids.cpu().numpy()
+    gpu_w = dev.w.cpu().numpy()
+    out = dev.out.cpu().numpy()
+    # routing of every token
+    ref_r = _oracle_routing(L, shape)
+    near = check_routing(gpu_ids, gpu_w, ref_r, shape)
+    # output rows of a sample whose GPU ids equal the oracle's
+    rows = _sample(T, n_check)
+    ref = orc.moe_layer_forward(L, shape, tokens=rows)
+    agree = [i for i, t in enumerate(rows) if sorted(gpu_ids[t]) == sorted(ref["ids"][i])]
+    assert len(agree) >= len(rows) - max(1, near)
+    tol = OUT_TOL[shape.act_dtype]
+    err = rel_rms_err(out[rows[agree]], ref["out"][agree])
+    y_err = rel_rms_err(out[rows[agree]] - L["r_attn"][rows[agree]],
+                        ref["out"][agree] - L["r_attn"][rows[agree]])
+    print("%s T=%d near-ties=%d out_err=%.3e y_moe_err=%.3e" % (shape.name, T, near, err, y_err))
+    assert err <= tol, err
+    assert y_err <= 10 * tol, y_err
+
+
+ROUTE_CASES = [(mi.TINY_F32, 32), (mi.QWEN36, 64), (mi.QWEN36_PREFILL_SKEW, 4096),
+               (mi.DEEPSEEK_GROUP, 4096), (mi.MIXTRAL, 2048)]
+
+
+@pytest.mark.parametrize("shape,T", ROUTE_CASES,
+                         ids=["%s-T%d" % (c[0].name, c[1]) for c in ROUTE_CASES])
+def test_route_parity_and_shared_gate(shape, T):
+    L = layer_host(shape, T)
+    dev = DevLayer(shape, L)
+    cfg = cfg_for(shape, T)
+    ws = smr.alloc_workspace(cfg)
+    s_sh = torch.empty(T, dtype=torch.float32, device="cuda") if shape.d_ff_shared else None
+    smr.route(cfg, ws, dev.t["x"], dev.t["W_router"], dev.ids, dev.w,
+              expert_bias=dev.t.get("expert_bias"), w_shared=dev.t.get("w_shared"),
+              s_shared=s_sh)
+    assert smr.read_device_status(cfg, ws)[0] == 0
+    ref = _oracle_routing(L, shape)
+    check_routing(dev.ids.cpu().numpy(), dev.w.cpu().numpy(), ref, shape)
+    if s_sh is not None:
+        x = orc.to_f64(L["x"], shape.act_dtype)
+        ws_ = orc.to_f64(L["w_shared"], shape.act_dtype)
+        want = np.array([orc.shared_gate(x[t], ws_) for t in range(T)])
+        np.testing.assert_allclose(s_sh.cpu().numpy(), want, atol=1e-5)
+
+
+BUCKET_CASES = [(1, 8, 256), (8, 8, 256), (64, 8, 256), (32, 4, 16), (37, 4, 16),
+                (4096, 8, 256), (4096, 8, 128), (2048, 2, 8), (5000, 3, 60), (1000, 32, 512)]
+
+
+@pytest.mark.parametrize("T,k,E", BUCKET_CASES)
+def test_bucket_parity(T, k, E):
+    rng = np.random.default_rng(T * 7 + k + E)
+    # skewed but valid ids (distinct per token)
+    p = rng.zipf(1.5, size=E).astype(np.float64)
+    p /= p.sum()
+    ids = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    ref = orc.bucket(ids, E)
+    cfg = smr.MoEConfig(T=T, d_model=64, n_experts=E, top_k=k, d_ff=64, d_ff_shared=0)
+    ws = smr.alloc_workspace(cfg)
+    i32 = lambda n: torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    counts, offsets, active, n_active = i32(E), i32(E + 1), i32(E), i32(4)
+    perm, pos = i32(T * k), i32(T * k)
+    smr.bucket(cfg, ws, to_dev(ids), counts, offsets, active, n_active, perm, pos)
+    assert smr.read_device_status(cfg, ws)[0] == 0
+    na = int(n_active[0])
+    assert na == len(ref["active"])
+    assert counts.cpu().numpy().tolist() == ref["counts"].tolist()
+    assert offsets.cpu().numpy().tolist() == ref["offsets"].tolist()
+    assert active.cpu().numpy()[:na].tolist() == ref["active"].tolist()
+    assert perm.cpu().numpy().tolist() == ref["perm"].tolist()
+    assert pos.cpu().numpy().tolist() == ref["pos"].tolist()
+
+
+def test_bucket_flags_out_of_range_ids():
+    T, k, E = 16, 4, 16
+    ids = np.arange(T * k, dtype=np.int32).reshape(T, k) % E
+    ids[3, 1] = E + 5
+    ids[7, 0] = -1
+    cfg = smr.MoEConfig(T=T, d_model=64, n_experts=E, top_k=k, d_ff=64, d_ff_shared=0)
+    ws = smr.alloc_workspace(cfg)
+    i32 = lambda n: torch.zeros((n,), dtype=torch.int32, device="cuda")
+    perm = i32(T * k)
+    smr.bucket(cfg, ws, to_dev(ids), i32(E), i32(E + 1), i32(E), i32(4), perm, i32(T * k))
+    st, word = smr.read_device_status(cfg, ws)
+    assert st == smr._STATUS.index("MOE_ERR_DEVICE_CHECK")
+    assert word & 1 and (word >> 16) == 1
+    # every access stayed in bounds: perm is still a permutation of the pairs
+    assert sorted(perm.cpu().numpy().tolist()) == list(range(T * k))
+    # the word was cleared by the read
+    assert smr.read_device_status(cfg, ws)[0] == 0
+
+
+EXPERT_CASES = [(mi.TINY_F32, 32, 32), (mi.QWEN36, 64, 64), (mi.DEEPSEEK_GROUP, 4096, 16)]
+
+
+@pytest.mark.parametrize("shape,T,n_check", EXPERT_CASES,
+                         ids=["%s-T%d" % (c[0].name, c[1]) for c in EXPERT_CASES])
+def test_experts_forward_parity_given_routing(shape, T, n_check):
+    """The expert half on its own, fed routing artefacts that do not come
+    from the GPU router (no near-tie can interfere)."""
+    L = layer_host(shape, T)
+    dev = DevLayer(shape, L)
+    ids, w, s = mi.random_router_outputs(shape, T)
+    cfg = cfg_for(shape, T)
+    ws = smr.alloc_workspace(cfg)
+    for gate_given in (False, True):
+        sh = dev.shared()
+        smr.experts_forward(cfg, ws, dev.t["x"], dev.t["r_attn"], to_dev(ids), to_dev(w),
+                            dev.bank("W_gate"), dev.bank("W_up"), dev.bank("W_down"), dev.out,
+                            s_shared=to_dev(s) if gate_given else None, **sh)
+        assert smr.read_device_status(cfg, ws)[0] == 0
+        rows = _sample(T, n_check, seed=3)
+        ref = orc.moe_experts_forward(L, shape, ids, w.astype(np.float64),
+                                      s.astype(np.float64) if gate_given else None, rows)
+        err = rel_rms_err(dev.out.cpu().numpy()[rows], ref["out"])
+        assert err <= OUT_TOL[shape.act_dtype], err
+
+
+def test_in_place_residual_update():
+    shape, T = mi.QWEN36, 8
+    L = layer_host(shape, T)
+    dev = DevLayer(shape, L)
+    cfg = cfg_for(shape, T)
+    ws = smr.alloc_workspace(cfg)
+    dev.layer_forward(cfg, ws)
+    want = dev.out.clone()
+    dev.out = dev.t["r_attn"]          # out aliases r_attn
+    dev.layer_forward(cfg, ws)
+    assert torch.equal(dev.t["r_attn"], want)
+
+
+def test_repeat_calls_are_deterministic():
+    shape, T = mi.QWEN36, 64
+    L = layer_host(shape, T)
+    dev = DevLayer(shape, L)
+    cfg = cfg_for(shape, T)
+    ws = smr.alloc_workspace(cfg)
+    dev.layer_forward(cfg, ws)
+    a = dev.out.clone()
+    ids = dev.ids.clone()
+    for _ in range(3):
+        dev.layer_forward(cfg, ws)
+        assert torch.equal(dev.out, a)
+        assert torch.equal(dev.ids, ids)
+
+
+def test_degenerate_shapes():
+    """k = E (every expert selected), E = 1 (dense), k = 1."""
+    for E, k in ((4, 4), (1, 1), (16, 1)):
+        shape = mi.TINY_F32.with_(name="deg", n_experts=E, top_k=k)
+        T = 9
+        L = mi.make_layer(shape, T)
+        dev = DevLayer(shape, L)
+        cfg = cfg_for(shape, T)
+        ws = smr.alloc_workspace(cfg)
+        dev.layer_forward(cfg, ws)
+        assert smr.read_device_status(cfg, ws)[0] == 0
+        ref = orc.moe_layer_forward(L, shape)
+        ids = dev.ids.cpu().numpy()
+        assert [sorted(r) for r in ids.tolist()] == [sorted(r) for r in ref["ids"].tolist()]
+        assert rel_rms_err(dev.out.cpu().numpy(), ref["out"]) <= OUT_TOL["f32"]
+
+
+def test_zero_tokens_is_a_no_op():
+    shape = mi.QWEN36
+    cfg = cfg_for(shape, 0)
+    ws = smr.alloc_workspace(cfg)
+    L = layer_host(shape, 1)
+    dev = DevLayer(shape, L)
+    empty = torch.empty((0, shape.d_model), dtype=torch.bfloat16, device="cuda")
+    smr.layer_forward(cfg, ws, empty, dev.t["r_attn"][:0], dev.t["W_router"],
+                      dev.bank("W_gate"), dev.bank("W_up"), dev.bank("W_down"),
+                      dev.out[:0], dev.ids[:0], dev.w[:0], **dev.shared())
+    assert smr.read_device_status(cfg, ws)[0] == 0
