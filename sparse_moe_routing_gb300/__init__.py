@@ -65,7 +65,14 @@ _SIGS = {
                                            _P, ctypes.POINTER(_Cfg), _P, _P]),
     "moe_layer_forward": (ctypes.c_int, [_P, _P, _P, _P, _Bank, _Bank, _Bank, _P, _P, _P, _P,
                                          ctypes.POINTER(_Cfg), _P, _P, _P, _P]),
+    "moe_launch_count": (ctypes.c_uint64, []),
+    "moe_trace_kernel": (ctypes.c_int, [ctypes.c_int, _P, _P, ctypes.c_int,
+                                        ctypes.POINTER(ctypes.c_int)]),
 }
+
+# kernel families (moe_kernel_t)
+KERNELS = {"router_logits": 1, "router_topk": 2, "shared_gate": 3, "bucket": 4,
+           "gemv_gateup": 5, "gemv_down": 6, "combine": 7, "tc_gateup": 8, "tc_down": 9}
 
 _lib = None
 
@@ -208,3 +215,79 @@ def layer_forward(cfg, workspace, x, r_attn, W_router, W_gate, W_up, W_down, out
         _bank(W_down), _ptr(Ws_gate), _ptr(Ws_up), _ptr(Ws_down), _ptr(w_shared),
         ctypes.byref(cfg._c(workspace)), _ptr(out), _ptr(topk_ids), _ptr(weights),
         _stream(stream)), "moe_layer_forward")
+
+
+def launch_count() -> int:
+    """Kernel launches this library has enqueued in this process."""
+    return int(lib().moe_launch_count())
+
+
+class KernelTrace:
+    """Brackets every launch of one kernel family with CUDA events recorded on
+    the stream it is launched on (moe_trace_kernel). Use as a context manager;
+    `durations_ms()` returns one duration per traced launch (up to n)."""
+
+    def __init__(self, kernel: str, n: int):
+        import torch
+        self.kernel = KERNELS[kernel]
+        self.n = n
+        self.starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        self.stops = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        self._count = ctypes.c_int(0)
+        # torch creates the CUDA event lazily: record once to materialise it
+        for e in self.starts + self.stops:
+            e.record()
+        self._sa = (ctypes.c_void_p * n)(*[e.cuda_event for e in self.starts])
+        self._so = (ctypes.c_void_p * n)(*[e.cuda_event for e in self.stops])
+
+    def __enter__(self):
+        _check(lib().moe_trace_kernel(self.kernel, self._sa, self._so, self.n,
+                                      ctypes.byref(self._count)), "moe_trace_kernel")
+        return self
+
+    def __exit__(self, *exc):
+        lib().moe_trace_kernel(0, None, None, 0, None)
+        return False
+
+    @property
+    def count(self) -> int:
+        return self._count.value
+
+    def durations_ms(self):
+        import torch
+        torch.cuda.synchronize()
+        m = min(self.count, self.n)
+        return [self.starts[i].elapsed_time(self.stops[i]) for i in range(m)]
+
+
+class MoELayer:
+    """One MoE layer's device weights plus its workspace: `forward` is the
+    call a user makes (x, r_attn device tensors in, out/ids/weights out).
+
+    weights: dict of device tensors named as in include/moe_route.h
+    (W_router, expert_bias, W_gate, W_up, W_down or (codes, scale, min)
+    tuples for 4-bit banks, Ws_gate, Ws_up, Ws_down, w_shared)."""
+
+    def __init__(self, cfg: MoEConfig, weights: dict, device=None):
+        import torch
+        self.cfg = cfg
+        self.w = weights
+        self.device = device or torch.device("cuda", torch.cuda.current_device())
+        self.ws = alloc_workspace(cfg, self.device)
+        T, k, d = cfg.T, cfg.top_k, cfg.d_model
+        self.out = torch.empty((T, d), dtype=torch.float32, device=self.device)
+        self.ids = torch.empty((T, k), dtype=torch.int32, device=self.device)
+        self.weights = torch.empty((T, k), dtype=torch.float32, device=self.device)
+
+    def forward(self, x, r_attn, out=None, stream=None):
+        w = self.w
+        out = self.out if out is None else out
+        layer_forward(self.cfg, self.ws, x, r_attn, w["W_router"], w["W_gate"], w["W_up"],
+                      w["W_down"], out, self.ids, self.weights,
+                      expert_bias=w.get("expert_bias"), Ws_gate=w.get("Ws_gate"),
+                      Ws_up=w.get("Ws_up"), Ws_down=w.get("Ws_down"),
+                      w_shared=w.get("w_shared"), stream=stream)
+        return out, self.ids, self.weights
+
+    def device_status(self, stream=None):
+        return read_device_status(self.cfg, self.ws, stream)

@@ -109,16 +109,26 @@ struct TraceState {
 
 // Runs one kernel launcher, counting it and bracketing it with the traced
 // events when its family is being traced.
+// While the stream is being captured into a CUDA graph, the records become
+// external event nodes, so every replay still timestamps the kernel.
+cudaError_t trace_record(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return cudaErrorUnknown;
+  if (cs == cudaStreamCaptureStatusActive)
+    return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  return cudaEventRecord(ev, st);
+}
+
 template <typename F>
 cudaError_t run(int kid, cudaStream_t st, F&& launch) {
   const bool tr = g_trace.kernel == kid && g_trace.n > 0;
   const int slot = tr ? (*g_trace.count % g_trace.n) : 0;
-  if (tr && cudaEventRecord(g_trace.starts[slot], st) != cudaSuccess) return cudaErrorUnknown;
+  if (tr && trace_record(g_trace.starts[slot], st) != cudaSuccess) return cudaErrorUnknown;
   cudaError_t e = launch();
   if (e != cudaSuccess) return e;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (tr) {
-    if (cudaEventRecord(g_trace.stops[slot], st) != cudaSuccess) return cudaErrorUnknown;
+    if (trace_record(g_trace.stops[slot], st) != cudaSuccess) return cudaErrorUnknown;
     ++*g_trace.count;
   }
   return cudaSuccess;

@@ -229,13 +229,9 @@ static cudaError_t launch_gateup_t(const GemvArgs& a, cudaStream_t st) {
   const int slots = a.routed_slots + (a.has_shared ? 1 : 0);
   const size_t smem = (size_t)kTok * kKc * sizeof(float);
   const int wmax = a.has_shared && a.Is > a.I ? a.Is : a.I;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_gateup_kernel<TW, TA>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static bool attr[64] = {};
+  cudaError_t e = ensure_smem_limit(gemv_gateup_kernel<TW, TA>, (int)smem, attr);
+  if (e != cudaSuccess) return e;
   gemv_gateup_kernel<TW, TA><<<dim3((wmax + kGuRows - 1) / kGuRows, slots), 256, smem, st>>>(a);
   return cudaGetLastError();
 }
@@ -244,13 +240,9 @@ template <typename TW>
 static cudaError_t launch_down_t(const GemvArgs& a, cudaStream_t st) {
   const int slots = a.routed_slots + (a.has_shared ? 1 : 0);
   const size_t smem = (size_t)kTok * kKc * sizeof(float);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_down_kernel<TW>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static bool attr[64] = {};
+  cudaError_t e = ensure_smem_limit(gemv_down_kernel<TW>, (int)smem, attr);
+  if (e != cudaSuccess) return e;
   gemv_down_kernel<TW><<<dim3((a.d + kDnRows - 1) / kDnRows, slots), 256, smem, st>>>(a);
   return cudaGetLastError();
 }

@@ -77,6 +77,20 @@ struct CombineArgs {
   int T, d, k;
 };
 
+// Raises `kernel`'s dynamic shared-memory opt-in limit to `bytes`, once per
+// device (flags: one per device ordinal, < 64).
+template <typename K>
+inline cudaError_t ensure_smem_limit(K kernel, int bytes, bool* flags) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (flags[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) flags[dev] = true;
+  return e;
+}
+
 // One launcher per kernel; each returns the launch's cudaError_t.
 cudaError_t launch_router_logits(const RouterArgs& ra, bool bf16, cudaStream_t st);
 cudaError_t launch_router_topk(const TopkArgs& ta, cudaStream_t st);

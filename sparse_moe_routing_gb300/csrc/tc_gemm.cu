@@ -1,0 +1,482 @@
+// Persistent grouped GEMM on the fifth-generation tensor cores (sm_103a):
+// TMA tile loads (128-byte swizzle) feed a 4-stage mbarrier pipeline, one
+// elected thread issues tcgen05.mma (bf16 x bf16 -> fp32) into a
+// double-buffered TMEM accumulator, and four epilogue warps drain TMEM with
+// tcgen05.ld and apply the fused epilogue while the next tile accumulates.
+//
+// Three uses, one kernel template:
+//  * gate/up ("How Treebeard routes Qwen3.6 MoE tokens", "Routed expert
+//    computation"; Edge0 "Experts"): per active expert, H = SiLU(X W_gate^T)
+//    * (X W_up^T); the gate and up tiles of the same 128 intermediate columns
+//    share one N = 256 instruction, so SwiGLU is applied straight from TMEM;
+//  * down: Y = alpha * (H W_down^T), the routing weight (or, for the shared
+//    expert, its sigmoid gate) applied in the epilogue;
+//  * router ("Routing math": z_t = W_router x_t) for large token batches:
+//    one dense problem, fp32 logits out.
+// Work items are (group, 128-row block, N tile); groups are the active
+// experts packed by the bucketing pass ("Intel SYCL path": launch over
+// active experts, load each weight block once per token block) plus the
+// shared expert as group E. CTAs stride over the item list.
+//
+// Every wait is bounded: a wait that exceeds about one second records
+// kDevTimeout in the workspace status word and the CTA winds down.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 epilogue
+constexpr uint32_t kTmemCols = 512;
+constexpr int kStageA = BM * BK * 2;      // 16 KB
+constexpr int kStageB = 256 * BK * 2;     // 32 KB (largest B tile)
+constexpr size_t kSmemBytes = 1024 + STAGES * (kStageA + kStageB) + 256;
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of `bar` with the given parity; false after ~1 s.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++n & 63u) == 0 && globaltimer() - t0 > 1000000000ull) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 128-byte-swizzled, K-major shared-memory matrix descriptor: rows of 128 B,
+// 8-row atoms 1024 B apart (stride byte offset), version bits for tcgen05.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both
+// K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+struct TileInfo {
+  int g, m, nt, row0, rows;
+  bool shared;
+};
+
+template <int MODE>
+__device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, int t) {
+  TileInfo ti;
+  const int rb = t / a.n_tiles;
+  ti.nt = t - rb * a.n_tiles;
+  if (MODE == kTcRouter) {
+    ti.g = 0;
+    ti.m = rb;
+    ti.row0 = 0;
+    ti.rows = a.T;
+    ti.shared = false;
+  } else {
+    const int2 r = a.rowblocks[rb];
+    ti.g = r.x;
+    ti.m = r.y;
+    if (ti.g < a.E) {
+      ti.row0 = a.offsets[ti.g];
+      ti.rows = a.offsets[ti.g + 1] - ti.row0;
+      ti.shared = false;
+    } else {
+      ti.row0 = 0;
+      ti.rows = a.T;
+      ti.shared = true;
+    }
+  }
+  return ti;
+}
+
+__device__ __forceinline__ void give_up(const TcArgs& a, volatile int* abort_flag, int site) {
+  *abort_flag = 1;
+  report(a.ctrl, kDevTimeout, site);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                   const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                   const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmB3,
+                   const TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * kStageA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * kStageB);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int site = MODE == kTcGateUp ? kSiteTcGateUp : (MODE == kTcDown ? kSiteTcDown : kSiteTcRouter);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int n_rb = MODE == kTcRouter ? (a.T + BM - 1) / BM : *a.n_rowblocks;
+  const int total = n_rb * a.n_tiles;
+  const int nkb = a.K / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      const uint32_t stage_bytes = kStageA + a.bn * BK * 2;
+      int stage = 0;
+      uint32_t ph = 0;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const TileInfo ti = decode_tile<MODE>(a, t);
+        const CUtensorMap* mA = ti.shared ? &tmA1 : &tmA0;
+        const CUtensorMap* mB0 = ti.shared ? &tmB2 : &tmB0;
+        const CUtensorMap* mB1 = ti.shared ? &tmB3 : &tmB1;
+        const int arow = ti.row0 + ti.m * BM;
+        const int bhalf = MODE == kTcGateUp ? a.bn / 2 : a.bn;
+        const int brow = (ti.shared || MODE == kTcRouter ? 0 : ti.g * a.brows_routed) +
+                         ti.nt * bhalf;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], ph ^ 1u)) {
+            give_up(a, abort_flag, site);
+            break;
+          }
+          mbar_expect_tx(&full[stage], stage_bytes);
+          uint8_t* b_dst = sB + stage * kStageB;
+          tma_load_2d(sA + stage * kStageA, mA, &full[stage], kb * BK, arow);
+          tma_load_2d(b_dst, mB0, &full[stage], kb * BK, brow);
+          if (MODE == kTcGateUp) tma_load_2d(b_dst + bhalf * BK * 2, mB1, &full[stage], kb * BK, brow);
+          if (++stage == STAGES) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_bf16(BM, a.bn);
+      int stage = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], aph ^ 1u)) {
+          give_up(a, abort_flag, site);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&full[stage], ph)) {
+            give_up(a, abort_flag, site);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * kStageA);
+          const uint32_t b_base = smem_u32(sB + stage * kStageB);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            mma_bf16(d_tmem, sw128_desc(a_base + k * 32), sw128_desc(b_base + k * 32), idesc,
+                     (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) aph ^= 1u;
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      const TileInfo ti = decode_tile<MODE>(a, t);
+      if (!mbar_wait(&tfull[acc], aph)) {
+        give_up(a, abort_flag, site);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(q * 32) << 16);
+      const int i = ti.m * BM + r;  // row inside the group
+      const bool valid = i < ti.rows;
+      if (MODE == kTcGateUp) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ti.shared ? a.out_shared : a.out_routed);
+        __nv_bfloat16* dst = out + (size_t)(ti.row0 + i) * a.ld_out + ti.nt * (a.bn / 2);
+        const int half = a.bn / 2;
+        for (int c0 = 0; c0 < half; c0 += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tbase + c0, g);
+          tmem_ld32(tbase + half + c0, u);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t h[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+              const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+              h[j] = pack_bf16x2(siluf_(g0) * u0, siluf_(g1) * u1);
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              st_global_v4(dst + c0 + 8 * v, h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+          }
+        }
+      } else if (MODE == kTcDown) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ti.shared ? a.out_shared : a.out_routed);
+        __nv_bfloat16* dst = out + (size_t)(ti.row0 + i) * a.ld_out + ti.nt * a.bn;
+        float scale = 0.f;
+        if (valid) scale = ti.shared ? a.s_shared[i] : a.alpha[a.perm[ti.row0 + i]];
+        for (int c0 = 0; c0 < a.bn; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c0, v);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t h[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              h[j] = pack_bf16x2(scale * __uint_as_float(v[2 * j]),
+                                 scale * __uint_as_float(v[2 * j + 1]));
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+              st_global_v4(dst + c0 + 8 * w, h[4 * w], h[4 * w + 1], h[4 * w + 2], h[4 * w + 3]);
+          }
+        }
+      } else {
+        float* out = static_cast<float*>(a.out_routed) + (size_t)i * a.ld_out;
+        for (int c0 = 0; c0 < a.bn; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c0, v);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) out[c0 + j] = __uint_as_float(v[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) {
+    // let copies and MMAs already in flight land before the CTA exits
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 2000000ull) {
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// X_perm[p] = x[perm[p] / k] (rows of the packed order, bf16)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
+                                                          const int32_t* __restrict__ perm, int k,
+                                                          int row_vecs, uint4* __restrict__ out,
+                                                          int P) {
+  for (int p = blockIdx.x; p < P; p += gridDim.x) {
+    const size_t src = (size_t)(perm[p] / k) * row_vecs;
+    const size_t dst = (size_t)p * row_vecs;
+    for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) out[dst + v] = __ldg(x + src + v);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2D bf16 view [rows][cols] (cols contiguous), box = 64 cols x box_rows rows,
+// 128-byte swizzle. A null or empty view yields a map over a 1-row dummy of
+// the same base that no tile ever addresses.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || !base) return false;
+  if (rows == 0) rows = 1;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (!n[dev]) cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev);
+  return n[dev] > 0 ? n[dev] : 1;
+}
+
+template <int MODE>
+cudaError_t launch_tc(const TcMaps& maps, const TcArgs& a, int max_items, cudaStream_t st) {
+  static bool attr[64] = {};
+  cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE>, (int)kSmemBytes, attr);
+  if (e != cudaSuccess) return e;
+  int grid = sm_count();
+  if (max_items < grid) grid = max_items;
+  if (grid < 1) grid = 1;
+  tc_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, st>>>(maps.A0, maps.A1, maps.B0, maps.B1,
+                                                           maps.B2, maps.B3, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows) {
+  return make_map(m, base, rows, cols, box_rows);
+}
+
+cudaError_t launch_tc_gemm(int mode, const TcMaps& maps, const TcArgs& a, int max_items,
+                           cudaStream_t st) {
+  if (mode == kTcGateUp) return launch_tc<kTcGateUp>(maps, a, max_items, st);
+  if (mode == kTcDown) return launch_tc<kTcDown>(maps, a, max_items, st);
+  return launch_tc<kTcRouter>(maps, a, max_items, st);
+}
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int d, void* out, int P,
+                               cudaStream_t st) {
+  if (P == 0) return cudaSuccess;
+  int grid = P < sm_count() * 16 ? P : sm_count() * 16;
+  gather_rows_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(x), perm, k, d / 8,
+                                          static_cast<uint4*>(out), P);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
