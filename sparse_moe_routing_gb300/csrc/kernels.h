@@ -1,6 +1,7 @@
 // Kernel argument blocks and launchers of the MoE layer (host + device).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -76,6 +77,41 @@ struct CombineArgs {
   float* out;               // [T][d]
   int T, d, k;
 };
+
+// Tensor-core grouped GEMM (tc_gemm.cu).
+enum TcMode { kTcGateUp = 0, kTcDown = 1, kTcRouter = 2 };
+
+struct TcArgs {
+  const int2* rowblocks;       // (group, m-tile) list from the bucketing pass
+  const int32_t* n_rowblocks;  // device count of row blocks
+  const int32_t* offsets;      // [E+1] packed-row offsets per routed expert
+  const int32_t* perm;         // packed row -> pair id
+  const float* alpha;          // [P] routing weights (down)
+  const float* s_shared;       // [T] shared gate (down)
+  void* out_routed;            // H | Y (bf16, packed rows) | logits (f32)
+  void* out_shared;            // Hs | Ys (bf16, token rows)
+  Ctrl* ctrl;
+  int E, T, K;                 // K: reduction length (multiple of 64)
+  int ld_out;                  // output row stride in elements
+  int n_tiles;                 // N tiles per row block
+  int bn;                      // N of one MMA (gate/up: 128 gate + 128 up)
+  int brows_routed;            // rows of one routed expert in the 2D B view
+};
+
+// The six operand maps: A routed/shared, B0/B1 routed, B2/B3 shared.
+struct TcMaps {
+  CUtensorMap A0, A1, B0, B1, B2, B3;
+};
+
+// Encodes a 2D bf16 TMA map [rows][cols] with a 64-column x box_rows box and
+// 128-byte swizzle; false if the driver entry point or the encoding fails.
+bool tc_make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows);
+cudaError_t launch_tc_gemm(int mode, const TcMaps& maps, const TcArgs& a, int max_items,
+                           cudaStream_t st);
+cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int d, void* out, int P,
+                               cudaStream_t st);
+int tc_sm_count();
 
 // Raises `kernel`'s dynamic shared-memory opt-in limit to `bytes`, once per
 // device (flags: one per device ordinal, < 64).

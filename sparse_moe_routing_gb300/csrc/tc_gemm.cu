@@ -435,7 +435,9 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
+}  // namespace
+
+int tc_sm_count() {
   static int n[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
@@ -443,12 +445,14 @@ int sm_count() {
   return n[dev] > 0 ? n[dev] : 1;
 }
 
+namespace {
+
 template <int MODE>
 cudaError_t launch_tc(const TcMaps& maps, const TcArgs& a, int max_items, cudaStream_t st) {
   static bool attr[64] = {};
   cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE>, (int)kSmemBytes, attr);
   if (e != cudaSuccess) return e;
-  int grid = sm_count();
+  int grid = tc_sm_count();
   if (max_items < grid) grid = max_items;
   if (grid < 1) grid = 1;
   tc_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, st>>>(maps.A0, maps.A1, maps.B0, maps.B1,
@@ -473,7 +477,7 @@ cudaError_t launch_tc_gemm(int mode, const TcMaps& maps, const TcArgs& a, int ma
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int d, void* out, int P,
                                cudaStream_t st) {
   if (P == 0) return cudaSuccess;
-  int grid = P < sm_count() * 16 ? P : sm_count() * 16;
+  int grid = P < tc_sm_count() * 16 ? P : tc_sm_count() * 16;
   gather_rows_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(x), perm, k, d / 8,
                                           static_cast<uint4*>(out), P);
   return cudaGetLastError();
