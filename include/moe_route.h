@@ -196,6 +196,25 @@ MOE_API moe_status_t moe_route(const void* x, const void* W_router,
                        const moe_cfg_t* cfg, int32_t* topk_ids, float* weights,
                        float* s_shared, void* stream);
 
+/* Routing without a workspace, for callers that cannot allocate device
+ * memory (a plugin whose host framework owns every allocation and offers no
+ * allocator; a serving loop that must not allocate once running, because an
+ * allocation can synchronise the device). The pages have no counterpart:
+ * this is a packaging of moe_route, with the same arguments, results and
+ * errors, except that the router logits live in a fixed array inside the
+ * library (4 MiB, held on every device that loads the library until exit)
+ * instead of cfg->workspace, which is ignored. Allocates nothing.
+ * - T * (E + 1) must not exceed 1,048,576 (MOE_ERR_UNSUPPORTED otherwise).
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ * - All calls share the array: calls whose kernels overlap on the GPU race
+ *   and must be serialised by the caller.
+ * - Its launches are not counted by moe_launch_count nor traced. */
+MOE_API moe_status_t moe_route_static(const void* x, const void* W_router,
+                                      const float* expert_bias, const void* w_shared,
+                                      const moe_cfg_t* cfg, int32_t* topk_ids, float* weights,
+                                      float* s_shared, void* stream);
+
 /* Counting and packing pass ("Intel SYCL path", steps 1-3 of the Treebeard
  * page) over given routing ids [T][k]: counts [E] pairs per expert, offsets
  * [E+1] exclusive scan, active [E] the experts with a pair in ascending id
