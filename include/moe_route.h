@@ -156,6 +156,10 @@ MOE_API int moe_abi_version(void);
 /* Human-readable name of a status code. Never NULL; static storage. */
 MOE_API const char* moe_status_string(moe_status_t status);
 
+/* Text of the last CUDA error behind a MOE_ERR_CUDA returned to the calling
+ * thread ("no error" if none). Static storage. */
+MOE_API const char* moe_last_cuda_error(void);
+
 /* Number of kernel launches this library has enqueued in this process (all
  * devices, all streams). For measurement: the difference across a region is
  * the number of this library's kernels launched in it. */

@@ -33,7 +33,13 @@ _STATUS = ["MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORK
 class MoEError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__("%s: %s" % (where, status_string(status)))
+        msg = "%s: %s" % (where, status_string(status))
+        if status == 4:
+            try:
+                msg += " (%s)" % lib().moe_last_cuda_error().decode()
+            except Exception:
+                pass
+        super().__init__(msg)
 
 
 class _Cfg(ctypes.Structure):
@@ -66,6 +72,7 @@ _SIGS = {
     "moe_layer_forward": (ctypes.c_int, [_P, _P, _P, _P, _Bank, _Bank, _Bank, _P, _P, _P, _P,
                                          ctypes.POINTER(_Cfg), _P, _P, _P, _P]),
     "moe_launch_count": (ctypes.c_uint64, []),
+    "moe_last_cuda_error": (ctypes.c_char_p, []),
     "moe_trace_kernel": (ctypes.c_int, [ctypes.c_int, _P, _P, ctypes.c_int,
                                         ctypes.POINTER(ctypes.c_int)]),
 }

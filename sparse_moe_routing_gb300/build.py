@@ -10,6 +10,7 @@ under csrc/ or include/, or this script is newer than its object.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import hashlib
 import os
 import shutil
 import subprocess
@@ -23,7 +24,12 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe_route.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
+# MOE_NVCC_EXTRA: extra nvcc flags for a special build (e.g. -DMOE_DEVICE_CHECKS);
+# objects of such a build go to their own folder.
+_EXTRA = os.environ.get("MOE_NVCC_EXTRA", "").split()
+if _EXTRA:
+    BUILD = BUILD + "_" + hashlib.sha1(" ".join(_EXTRA).encode()).hexdigest()[:8]
+NVCC_FLAGS = _EXTRA + ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",
                      "-I" + INCLUDE, "-I" + CSRC]
 

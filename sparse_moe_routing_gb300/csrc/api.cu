@@ -77,6 +77,8 @@ moe_status_t validate_cfg(const moe_cfg_t* c) {
   if (c->n_experts > 512 || c->top_k > 32) return MOE_ERR_UNSUPPORTED;
   if (c->expert_dtype == MOE_F32 && c->act_dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
   if (c->expert_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (!gemv_supported(c->d_model, c->d_ff > c->d_ff_shared ? c->d_ff : c->d_ff_shared))
+    return MOE_ERR_UNSUPPORTED;
   if (c->expert_dtype == MOE_Q4_AFFINE_G64) return MOE_ERR_UNSUPPORTED;  // not built yet
   if (c->path == MOE_PATH_TC) return MOE_ERR_UNSUPPORTED;                // not built yet
   return MOE_OK;
@@ -93,7 +95,14 @@ T* at(const moe_cfg_t* c, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(c->workspace) + off);
 }
 
-moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+// Last CUDA error seen by a call of this thread (moe_last_cuda_error).
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+moe_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  g_last_cuda_error = e;
+  return MOE_ERR_CUDA;
+}
 
 // ---------------------------------------------------------------------------
 // measurement: launch counter and optional event bracketing of one kernel
@@ -125,7 +134,10 @@ cudaError_t run(int kid, cudaStream_t st, F&& launch) {
   const int slot = tr ? (*g_trace.count % g_trace.n) : 0;
   if (tr && trace_record(g_trace.starts[slot], st) != cudaSuccess) return cudaErrorUnknown;
   cudaError_t e = launch();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) {
+    g_last_cuda_error = e;
+    return e;
+  }
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (tr) {
     if (trace_record(g_trace.stops[slot], st) != cudaSuccess) return cudaErrorUnknown;
@@ -249,6 +261,8 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* moe_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 
 moe_status_t moe_trace_kernel(int kernel, void* const* starts, void* const* stops, int n,
                               int* count) {

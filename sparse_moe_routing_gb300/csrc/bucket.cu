@@ -148,10 +148,9 @@ cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t st) {
   const int words = kBucketWarps * a.E + a.E + (a.E + 1) + a.E + (a.E + 1) +
                     3 * (a.E + 1) + 1;
   const size_t smem = (size_t)words * sizeof(int);
-  // raise the opt-in limit once per device to the largest size any E needs
-  static bool attr[64] = {};
-  const int max_words = kBucketWarps * 512 + 4 * 513 + 3 * 513 + 1;
-  cudaError_t e = ensure_smem_limit(bucket_kernel, (int)(max_words * sizeof(int)), attr);
+  // raise the opt-in limit when this E needs more than the default
+  static int attr[64] = {};
+  cudaError_t e = ensure_smem_limit(bucket_kernel, (int)smem, attr);
   if (e != cudaSuccess) return e;
   bucket_kernel<<<1, kBucketThreads, smem, st>>>(a);
   return cudaGetLastError();

@@ -1,0 +1,41 @@
+// Unpermute-combine and residual ("How Treebeard routes Qwen3.6 MoE tokens",
+// "Shared expert computation" and "Pseudocode": r_next = r_attention +
+// (y_routed + y_shared); Airframe roadmap "Expert Combine": output = sum of
+// weight_k * expert_k_output). The routing weights and the shared gate were
+// already applied by the down projection, so each output row is
+//   out[t] = r_attn[t] + ((sum over slots s, in slot order, of Y[pos[t*k+s]]) + Ys[t]),
+// a fixed summation order (deterministic). One thread per float4 column.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// out[t] = r_attn[t] + ((sum over slots of Y[pos[t*k+s]]) + Ys[t])
+__global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+  const int t = blockIdx.x;
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;  // float4 column
+  if (c * 4 >= a.d) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < a.k; ++s) {
+    const int p = a.pos[(size_t)t * a.k + s];
+    const float4 y = reinterpret_cast<const float4*>(a.Y + (size_t)p * a.d)[c];
+    acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
+  }
+  if (a.Ys) {
+    const float4 y = reinterpret_cast<const float4*>(a.Ys + (size_t)t * a.d)[c];
+    acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
+  }
+  const float4 r = reinterpret_cast<const float4*>(a.r_attn + (size_t)t * a.d)[c];
+  float4 o;
+  o.x = r.x + acc.x; o.y = r.y + acc.y; o.z = r.z + acc.z; o.w = r.w + acc.w;
+  reinterpret_cast<float4*>(a.out + (size_t)t * a.d)[c] = o;
+}
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
+  if (a.T == 0) return cudaSuccess;
+  const int cols = a.d / 4;
+  combine_kernel<<<dim3(a.T, (cols + 255) / 256), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

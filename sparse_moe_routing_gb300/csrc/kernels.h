@@ -59,8 +59,8 @@ struct GemvArgs {
   const void* Wu_scale; const void* Wu_min;
   const void* Wd_scale; const void* Wd_min;
   const void* Wsg; const void* Wsu; const void* Wsd;           // shared expert
-  float* H;                 // [P][I] f32
-  float* Hs;                // [T][Is] f32
+  void* H;                  // [P][I] weight dtype (bf16 or f32)
+  void* Hs;                 // [T][Is] weight dtype
   float* Y;                 // [P][d] f32 (alpha applied)
   float* Ys;                // [T][d] f32 (s_shared applied)
   Ctrl* ctrl;
@@ -113,17 +113,18 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int d,
                                cudaStream_t st);
 int tc_sm_count();
 
-// Raises `kernel`'s dynamic shared-memory opt-in limit to `bytes`, once per
-// device (flags: one per device ordinal, < 64).
+// Raises `kernel`'s dynamic shared-memory opt-in limit to at least `bytes`
+// on the current device; `limits` holds the value set so far per device
+// ordinal (< 64), so the attribute is only set when a launch needs more.
 template <typename K>
-inline cudaError_t ensure_smem_limit(K kernel, int bytes, bool* flags) {
+inline cudaError_t ensure_smem_limit(K kernel, int bytes, int* limits) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (flags[dev]) return cudaSuccess;
+  if (bytes <= 48 * 1024 || limits[dev] >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) flags[dev] = true;
+  if (e == cudaSuccess) limits[dev] = bytes;
   return e;
 }
 
@@ -135,6 +136,8 @@ cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t st);
 // act: 0 f32, 1 bf16; wdt: 0 f32, 1 bf16, 2 q4
 cudaError_t launch_gemv_gateup(const GemvArgs& a, int act, int wdt, cudaStream_t st);
 cudaError_t launch_gemv_down(const GemvArgs& a, int act, int wdt, cudaStream_t st);
+// True when the GEMV kernels can stage at least one token of width d and kmax.
+bool gemv_supported(int d, int kmax);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 
 }  // namespace moe

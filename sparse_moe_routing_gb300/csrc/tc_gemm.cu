@@ -223,59 +223,72 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = n_rb * a.n_tiles;
   const int nkb = a.K / BK;
 
+  // Every role loop below is run by its whole warp, so that each warp reaches
+  // the closing CTA barrier converged; lane 0 issues the TMA copies and the
+  // MMAs. A wait's outcome is lane 0's, broadcast to the warp.
   if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      const uint32_t stage_bytes = kStageA + a.bn * BK * 2;
-      int stage = 0;
-      uint32_t ph = 0;
-      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-        const TileInfo ti = decode_tile<MODE>(a, t);
-        const CUtensorMap* mA = ti.shared ? &tmA1 : &tmA0;
-        const CUtensorMap* mB0 = ti.shared ? &tmB2 : &tmB0;
-        const CUtensorMap* mB1 = ti.shared ? &tmB3 : &tmB1;
-        const int arow = ti.row0 + ti.m * BM;
-        const int bhalf = MODE == kTcGateUp ? a.bn / 2 : a.bn;
-        const int brow = (ti.shared || MODE == kTcRouter ? 0 : ti.g * a.brows_routed) +
-                         ti.nt * bhalf;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&empty[stage], ph ^ 1u)) {
-            give_up(a, abort_flag, site);
-            break;
-          }
+    // -------------------------------------------------------------- producer
+    const uint32_t stage_bytes = kStageA + a.bn * BK * 2;
+    int stage = 0;
+    uint32_t ph = 0;
+    bool alive = true;
+    for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
+      const TileInfo ti = decode_tile<MODE>(a, t);
+      const CUtensorMap* mA = ti.shared ? &tmA1 : &tmA0;
+      const CUtensorMap* mB0 = ti.shared ? &tmB2 : &tmB0;
+      const CUtensorMap* mB1 = ti.shared ? &tmB3 : &tmB1;
+      const int arow = ti.row0 + ti.m * BM;
+      const int bhalf = MODE == kTcGateUp ? a.bn / 2 : a.bn;
+      const int brow = (ti.shared || MODE == kTcRouter ? 0 : ti.g * a.brows_routed) +
+                       ti.nt * bhalf;
+      for (int kb = 0; kb < nkb; ++kb) {
+        bool ok = lane == 0 ? mbar_wait(&empty[stage], ph ^ 1u) : true;
+        ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
+        if (!ok) {
+          if (lane == 0) give_up(a, abort_flag, site);
+          alive = false;
+          break;
+        }
+        if (lane == 0) {
           mbar_expect_tx(&full[stage], stage_bytes);
           uint8_t* b_dst = sB + stage * kStageB;
           tma_load_2d(sA + stage * kStageA, mA, &full[stage], kb * BK, arow);
           tma_load_2d(b_dst, mB0, &full[stage], kb * BK, brow);
-          if (MODE == kTcGateUp) tma_load_2d(b_dst + bhalf * BK * 2, mB1, &full[stage], kb * BK, brow);
-          if (++stage == STAGES) {
-            stage = 0;
-            ph ^= 1u;
-          }
+          if (MODE == kTcGateUp)
+            tma_load_2d(b_dst + bhalf * BK * 2, mB1, &full[stage], kb * BK, brow);
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          ph ^= 1u;
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_bf16(BM, a.bn);
-      int stage = 0, acc = 0;
-      uint32_t ph = 0, aph = 0;
-      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], aph ^ 1u)) {
-          give_up(a, abort_flag, site);
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16(BM, a.bn);
+    int stage = 0, acc = 0;
+    uint32_t ph = 0, aph = 0;
+    bool alive = true;
+    for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
+      bool ok = lane == 0 ? mbar_wait(&tempty[acc], aph ^ 1u) : true;
+      ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
+      if (!ok) {
+        if (lane == 0) give_up(a, abort_flag, site);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+      for (int kb = 0; kb < nkb; ++kb) {
+        ok = lane == 0 ? mbar_wait(&full[stage], ph) : true;
+        ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
+        if (!ok) {
+          if (lane == 0) give_up(a, abort_flag, site);
+          alive = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full[stage], ph)) {
-            give_up(a, abort_flag, site);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        if (lane == 0) {
           const uint32_t a_base = smem_u32(sA + stage * kStageA);
           const uint32_t b_base = smem_u32(sB + stage * kStageB);
 #pragma unroll
@@ -284,16 +297,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                      (kb | k) != 0 ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            ph ^= 1u;
-          }
         }
-        if (!ok) break;
-        mma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) aph ^= 1u;
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          ph ^= 1u;
+        }
       }
+      if (!alive) break;
+      if (lane == 0) mma_commit(&tfull[acc]);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
     }
   } else {
     // -------------------------------------------------------------- epilogue
@@ -303,8 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
       const TileInfo ti = decode_tile<MODE>(a, t);
-      if (!mbar_wait(&tfull[acc], aph)) {
-        give_up(a, abort_flag, site);
+      bool ok = lane == 0 ? mbar_wait(&tfull[acc], aph) : true;
+      ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
+      if (!ok) {
+        if (lane == 0) give_up(a, abort_flag, site);
         break;
       }
       tc_fence_after();
@@ -449,7 +466,7 @@ namespace {
 
 template <int MODE>
 cudaError_t launch_tc(const TcMaps& maps, const TcArgs& a, int max_items, cudaStream_t st) {
-  static bool attr[64] = {};
+  static int attr[64] = {};
   cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE>, (int)kSmemBytes, attr);
   if (e != cudaSuccess) return e;
   int grid = tc_sm_count();
