@@ -147,7 +147,8 @@ typedef enum {
   MOE_KERNEL_GEMV_DOWN = 6,     /* streaming down x alpha */
   MOE_KERNEL_COMBINE = 7,       /* unpermute, shared branch, residual */
   MOE_KERNEL_TC_GATEUP = 8,     /* tensor-core grouped gate/up + SwiGLU */
-  MOE_KERNEL_TC_DOWN = 9        /* tensor-core grouped down x alpha */
+  MOE_KERNEL_TC_DOWN = 9,       /* tensor-core grouped down x alpha */
+  MOE_KERNEL_GATHER = 10        /* packed-row gather of x (tensor-core path) */
 } moe_kernel_t;
 
 /* Returns the ABI version (MOE_ROUTE_ABI_VERSION). */

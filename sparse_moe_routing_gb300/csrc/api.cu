@@ -19,8 +19,26 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct Plan {
   size_t ctrl, logits, s_shared, counts, offsets, active, perm, pos, rowblocks;
-  size_t H, Hs, Y, Ys, total;
+  size_t H, Hs, Y, Ys, Xperm, total;
 };
+
+// Token batches at or above this size take the tensor-core path under
+// MOE_PATH_AUTO (when the shape allows it).
+constexpr int kTcMinTokens = 16;
+
+// The tensor-core path: bf16 experts and activations, K dims multiples of the
+// 64-element TMA box, N tiles of 128 (gate/up) and 256 (down), and a shared
+// expert (if any) as wide as the routed ones.
+bool tc_shape_ok(const moe_cfg_t& c) {
+  return c.expert_dtype == MOE_BF16 && c.act_dtype == MOE_BF16 && c.d_model % 256 == 0 &&
+         c.d_ff % 128 == 0 && (c.d_ff_shared == 0 || c.d_ff_shared == c.d_ff);
+}
+
+bool use_tc(const moe_cfg_t& c) {
+  if (!tc_shape_ok(c)) return false;
+  if (c.path == MOE_PATH_TC) return true;
+  return c.path == MOE_PATH_AUTO && c.T >= kTcMinTokens;
+}
 
 Plan make_plan(const moe_cfg_t& c) {
   Plan p{};
@@ -45,6 +63,7 @@ Plan make_plan(const moe_cfg_t& c) {
   p.Hs = take(T * Is * 4);
   p.Y = take(P * d * 4);
   p.Ys = take(Is ? T * d * 4 : 0);
+  p.Xperm = take(tc_shape_ok(c) ? P * d * 2 : 0);
   p.total = off;
   return p;
 }
@@ -80,7 +99,7 @@ moe_status_t validate_cfg(const moe_cfg_t* c) {
   if (!gemv_supported(c->d_model, c->d_ff > c->d_ff_shared ? c->d_ff : c->d_ff_shared))
     return MOE_ERR_UNSUPPORTED;
   if (c->expert_dtype == MOE_Q4_AFFINE_G64) return MOE_ERR_UNSUPPORTED;  // not built yet
-  if (c->path == MOE_PATH_TC) return MOE_ERR_UNSUPPORTED;                // not built yet
+  if (c->path == MOE_PATH_TC && !tc_shape_ok(*c)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -195,13 +214,108 @@ moe_status_t enqueue_bucket(const int32_t* ids, const moe_cfg_t* c, int32_t* cou
   b.P = c->T * c->top_k;
   b.E = c->n_experts;
   b.rowblocks = nullptr;
+  if (use_tc(*c)) {
+    // the tensor-core path walks (group, 128-row block) work items
+    const Plan p = make_plan(*c);
+    b.rowblocks = at<int2>(c, p.rowblocks);
+    b.n_rowblocks = &at<Ctrl>(c, 0)->n_rowblocks;
+    b.bm = kTcBm;
+    b.shared_rows = c->d_ff_shared > 0 ? c->T : 0;
+  }
   return cuda_status(run(MOE_KERNEL_BUCKET, st, [&] { return launch_bucket(b, st); }));
+}
+
+// Tensor-core sequence: gather X_perm, grouped gate/up (+SwiGLU) and down
+// (x alpha) GEMMs over the (group, row block, N tile) items, bf16 combine.
+moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float* alpha,
+                                const float* s_shared, moe_bank_t Wg, moe_bank_t Wu,
+                                moe_bank_t Wd, const void* Wsg, const void* Wsu, const void* Wsd,
+                                const moe_cfg_t* c, float* out, cudaStream_t st) {
+  const Plan p = make_plan(*c);
+  Ctrl* ctrl = at<Ctrl>(c, 0);
+  const int T = c->T, d = c->d_model, E = c->n_experts, k = c->top_k, I = c->d_ff;
+  const int Is = c->d_ff_shared, P = T * k;
+  const bool shared = Is > 0;
+  void* xperm = at<void>(c, p.Xperm);
+  void* H = at<void>(c, p.H);
+  void* Hs = at<void>(c, p.Hs);
+  void* Y = at<void>(c, p.Y);
+  void* Ys = at<void>(c, p.Ys);
+  const int32_t* perm = at<int32_t>(c, p.perm);
+
+  cudaError_t e = run(MOE_KERNEL_GATHER, st,
+                      [&] { return launch_gather_rows(x, perm, k, d, xperm, P, st); });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  const int max_rb = (P + kTcBm - 1) / kTcBm + (P < E ? P : E) + 1 +
+                     (shared ? (T + kTcBm - 1) / kTcBm + 1 : 0);
+  TcArgs a{};
+  a.rowblocks = at<int2>(c, p.rowblocks);
+  a.n_rowblocks = &ctrl->n_rowblocks;
+  a.offsets = at<int32_t>(c, p.offsets);
+  a.perm = perm;
+  a.alpha = alpha;
+  a.s_shared = s_shared;
+  a.ctrl = ctrl;
+  a.E = E;
+  a.T = T;
+
+  // gate/up: A = X_perm (routed) / x (shared), B = gate and up rows
+  TcMaps m{};
+  bool ok = tc_make_map(&m.A0, xperm, P, d, 128) && tc_make_map(&m.A1, x, T, d, 128) &&
+            tc_make_map(&m.B0, Wg.w, (uint64_t)E * I, d, 128) &&
+            tc_make_map(&m.B1, Wu.w, (uint64_t)E * I, d, 128);
+  if (ok && shared) ok = tc_make_map(&m.B2, Wsg, Is, d, 128) && tc_make_map(&m.B3, Wsu, Is, d, 128);
+  if (!ok) return MOE_ERR_CUDA;
+  if (!shared) {
+    m.B2 = m.B0;
+    m.B3 = m.B1;
+  }
+  a.out_routed = H;
+  a.out_shared = Hs;
+  a.K = d;
+  a.ld_out = I;
+  a.n_tiles = I / 128;
+  a.bn = 256;
+  a.brows_routed = I;
+  e = run(MOE_KERNEL_TC_GATEUP, st,
+          [&] { return launch_tc_gemm(kTcGateUp, m, a, max_rb * a.n_tiles, st); });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // down: A = H (routed) / Hs (shared), B = down rows; alpha in the epilogue
+  TcMaps m2{};
+  ok = tc_make_map(&m2.A0, H, P, I, 128) && tc_make_map(&m2.B0, Wd.w, (uint64_t)E * d, I, 256);
+  if (ok && shared) ok = tc_make_map(&m2.A1, Hs, T, Is, 128) && tc_make_map(&m2.B2, Wsd, d, Is, 256);
+  if (!ok) return MOE_ERR_CUDA;
+  if (!shared) {
+    m2.A1 = m2.A0;
+    m2.B2 = m2.B0;
+  }
+  m2.B1 = m2.B0;
+  m2.B3 = m2.B2;
+  a.out_routed = Y;
+  a.out_shared = Ys;
+  a.K = I;
+  a.ld_out = d;
+  a.n_tiles = d / 256;
+  a.bn = 256;
+  a.brows_routed = d;
+  e = run(MOE_KERNEL_TC_DOWN, st,
+          [&] { return launch_tc_gemm(kTcDown, m2, a, max_rb * a.n_tiles, st); });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  CombineArgs cb{r_attn, static_cast<const float*>(Y),
+                 shared ? static_cast<const float*>(Ys) : nullptr, at<int32_t>(c, p.pos), out,
+                 T, d, k, 1};
+  return cuda_status(run(MOE_KERNEL_COMBINE, st, [&] { return launch_combine(cb, st); }));
 }
 
 moe_status_t enqueue_experts(const void* x, const float* r_attn, const float* alpha,
                              const float* s_shared, moe_bank_t Wg, moe_bank_t Wu, moe_bank_t Wd,
                              const void* Wsg, const void* Wsu, const void* Wsd,
                              const moe_cfg_t* c, float* out, cudaStream_t st) {
+  if (use_tc(*c))
+    return enqueue_experts_tc(x, r_attn, alpha, s_shared, Wg, Wu, Wd, Wsg, Wsu, Wsd, c, out, st);
   const Plan p = make_plan(*c);
   Ctrl* ctrl = at<Ctrl>(c, 0);
   GemvArgs g{};
@@ -234,7 +348,7 @@ moe_status_t enqueue_experts(const void* x, const float* r_attn, const float* al
   e = run(MOE_KERNEL_GEMV_DOWN, st, [&] { return launch_gemv_down(g, act, wdt, st); });
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   CombineArgs cb{r_attn, g.Y, g.has_shared ? g.Ys : nullptr, at<int32_t>(c, p.pos), out,
-                 c->T, c->d_model, c->top_k};
+                 c->T, c->d_model, c->top_k, 0};
   return cuda_status(run(MOE_KERNEL_COMBINE, st, [&] { return launch_combine(cb, st); }));
 }
 
@@ -270,7 +384,7 @@ moe_status_t moe_trace_kernel(int kernel, void* const* starts, void* const* stop
     g_trace = TraceState{};
     return MOE_OK;
   }
-  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_TC_DOWN || n <= 0 || !starts ||
+  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_GATHER || n <= 0 || !starts ||
       !stops || !count)
     return MOE_ERR_INVALID_ARG;
   g_trace.kernel = kernel;

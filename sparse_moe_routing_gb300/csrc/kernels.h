@@ -71,11 +71,12 @@ struct GemvArgs {
 
 struct CombineArgs {
   const float* r_attn;      // [T][d]
-  const float* Y;           // [P][d]
-  const float* Ys;          // [T][d] or null
+  const float* Y;           // [P][d] f32, or bf16 when y_bf16
+  const float* Ys;          // [T][d] or null (same dtype as Y)
   const int32_t* pos;       // [P]
   float* out;               // [T][d]
   int T, d, k;
+  int y_bf16;
 };
 
 // Tensor-core grouped GEMM (tc_gemm.cu).

@@ -255,3 +255,32 @@ def test_zero_tokens_is_a_no_op():
                       dev.bank("W_gate"), dev.bank("W_up"), dev.bank("W_down"),
                       dev.out[:0], dev.ids[:0], dev.w[:0], **dev.shared())
     assert smr.read_device_status(cfg, ws)[0] == 0
+
+
+# A small shape whose experts each hold several 128-row tiles with a ragged
+# tail (E = 4, k = 2, T = 400: ~200 rows per expert), two N tiles of gate/up
+# (I = 256) and two of down (d = 512), with a full fp64 oracle.
+TC_SMALL = mi.MoEShape("tc_small", 7, d_model=512, n_experts=4, top_k=2, d_ff=256,
+                       d_ff_shared=256, tokens=(400,))
+PATH_CASES = [(TC_SMALL, 400), (TC_SMALL, 37), (TC_SMALL, 1), (mi.QWEN36, 64),
+              (mi.DEEPSEEK_GROUP, 37)]
+
+
+@pytest.mark.parametrize("path", [smr.PATH_GEMV, smr.PATH_TC], ids=["gemv", "tc"])
+@pytest.mark.parametrize("shape,T", PATH_CASES,
+                         ids=["%s-T%d" % (c[0].name, c[1]) for c in PATH_CASES])
+def test_both_expert_paths_match_oracle(shape, T, path):
+    """The CUDA-core streaming path and the tcgen05 grouped-GEMM path, each
+    forced, against the oracle on every output row."""
+    L, dev, cfg, ws = _run_layer(shape, T, path)
+    ref = orc.moe_layer_forward(L, shape)
+    ids = dev.ids.cpu().numpy()
+    near = check_routing(ids, dev.w.cpu().numpy(), ref, shape)
+    agree = [t for t in range(T) if sorted(ids[t]) == sorted(ref["ids"][t])]
+    assert len(agree) >= T - max(1, near)
+    out = dev.out.cpu().numpy()
+    err = rel_rms_err(out[agree], ref["out"][agree])
+    y_err = rel_rms_err(out[agree] - L["r_attn"][agree], ref["out"][agree] - L["r_attn"][agree])
+    print("%s T=%d path=%d out_err=%.3e y_moe_err=%.3e" % (shape.name, T, path, err, y_err))
+    assert err <= OUT_TOL[shape.act_dtype]
+    assert y_err <= 10 * OUT_TOL[shape.act_dtype]
