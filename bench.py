@@ -1,12 +1,14 @@
 #!/usr/bin/env python
 """Throughput of the sparse MoE layer forward on GB300 (tokens/s).
 
-Workload: the Qwen3.6-35B-A3B MoE layer shape (d_model 2048, 256 routed
-experts, top-8 softmax with renormalisation, expert and shared intermediate
-512, one sigmoid-gated shared expert), synthetic seeded weights N(0, 0.02)
-in bf16 and RMS-normalised activations, at the decode batch T (default 64;
-the sweep also runs T = 1 and 8). One step = one full layer forward (router,
+Default workload: the Qwen3.6-35B-A3B MoE layer shape (d_model 2048, 256
+routed experts, top-8 softmax with renormalisation, expert and shared
+intermediate 512, one sigmoid-gated shared expert), synthetic seeded weights
+N(0, 0.02) in bf16 and RMS-normalised activations, at the decode batch T=64
+(the sweep also runs T = 1 and 8). One step = one full layer forward (router,
 routing rule, bucketing, routed experts, shared expert, combine, residual).
+Other workloads (--workload prefill | deepseek | mixtral) run the other
+shapes of the same family for measurement; the default is the headline.
 
 Timing: K steps are captured into one CUDA graph and replayed (W eager
 warm-up steps first). Consecutive steps use distinct copies of the layer's
@@ -16,7 +18,9 @@ stream bracket the replay; the dominant kernel is additionally bracketed by
 events inside the graph (moe_trace_kernel) for the roofline figure.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--tokens T]
-                       [--impl ours|reference] [--no-sweep] [--no-cpu-baseline]
+                       [--workload decode|prefill|deepseek|mixtral]
+                       [--path auto|gemv|tc] [--impl ours|reference]
+                       [--no-sweep] [--no-cpu-baseline]
 For N > 1 launch with torchrun (one rank per GPU, NCCL): every rank runs an
 independent replica on its own token batch (the layer has no cross-token
 exchange), so the job processes N*T tokens per step ("scaling": "weak").
@@ -39,6 +43,16 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s (Qwen3.6 shape, T=1..4096); % of HBM/tensor roofline"
 L2_BYTES = 129 * 10 ** 6
+TC_MIN_TOKENS = 4  # the library's MOE_PATH_AUTO switch to the tensor-core path
+
+WORKLOADS = {
+    # name: (preset, default T, description)
+    "decode": ("qwen36_decode", 64, "qwen3.6-35b-a3b moe layer forward, decode batch T=%d"),
+    "prefill": ("qwen36_prefill_skew", 4096,
+                "qwen3.6-35b-a3b moe layer forward, prefill T=%d, skewed routing"),
+    "deepseek": ("deepseek_group", 4096, "deepseek-style sigmoid group top-k layer, T=%d"),
+    "mixtral": ("mixtral_bf16", 2048, "mixtral-style top-2 layer, bf16, T=%d"),
+}
 
 
 def _peaks():
@@ -51,11 +65,15 @@ def _peaks():
 
 
 # ----------------------------------------------------------------------------
-# algorithmic work (what the layer must move; intermediates excluded)
+# algorithmic work (what the layer must move / compute; intermediates excluded)
 # ----------------------------------------------------------------------------
+def _wbytes(shape):
+    return 2 if shape.expert_dtype == "bf16" else 4
+
+
 def layer_bytes(shape, T, n_active):
     d, E, I, Is, k = shape.d_model, shape.n_experts, shape.d_ff, shape.d_ff_shared, shape.top_k
-    wb = 2  # bf16
+    wb = _wbytes(shape)
     b = E * d * wb + (d * wb if Is else 0)                 # router (+ shared gate)
     b += n_active * 3 * I * d * wb + 3 * Is * d * wb       # active experts + shared expert
     b += T * d * wb + 2 * T * d * 4 + T * k * 8            # x, r_attn, out, ids+weights
@@ -67,12 +85,16 @@ def layer_flops(shape, T):
     return 2 * T * d * (E + (1 if Is else 0)) + 2 * T * k * 3 * d * I + 2 * T * 3 * d * Is
 
 
-def gateup_bytes(shape, T, n_active):
-    """Per launch of the gate/up kernel: the gate and up rows of every active
-    expert and of the shared expert (4,194,304 B each at this shape), plus the
-    activations x."""
-    d, I, Is = shape.d_model, shape.d_ff, shape.d_ff_shared
-    return n_active * 2 * I * d * 2 + 2 * Is * d * 2 + T * d * 2
+def gateup_work(shape, T, n_active):
+    """Per launch of a gate/up kernel: the gate and up rows of every active
+    expert and of the shared expert (2*I*d*2 B each: 4,194,304 B at the Qwen
+    shape) plus the activations x; flops 2*d*2*I per routed pair and per
+    shared row."""
+    d, I, Is, k = shape.d_model, shape.d_ff, shape.d_ff_shared, shape.top_k
+    wb = _wbytes(shape)
+    b = n_active * 2 * I * d * wb + 2 * Is * d * wb + T * d * wb
+    f = 2 * T * k * d * 2 * I + 2 * T * d * 2 * Is
+    return b, f
 
 
 # ----------------------------------------------------------------------------
@@ -116,9 +138,8 @@ class ClockSampler:
         rows = []
         for ts, line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            rows.append((ts, parts))
+            if len(parts) >= 9:
+                rows.append((ts, parts))
         if not rows:
             return None
         inside = [r for r in rows if t0 <= r[0] <= t1 + 0.05]
@@ -147,8 +168,8 @@ def _to_dev(a, device):
 
 
 def _traffic(kernel_name):
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current source of that kernel (else None)."""
+    """dram bytes per unit from the committed ncu summary, if it was taken on
+    the current source of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -178,26 +199,40 @@ class Weights:
         return self.copies[:n]
 
 
+def _cfg(shape, T, path):
+    import sparse_moe_routing_gb300 as smr
+    dt = {"f32": smr.F32, "bf16": smr.BF16, "q4": smr.Q4_AFFINE_G64}
+    return smr.MoEConfig(
+        T=T, d_model=shape.d_model, n_experts=shape.n_experts, top_k=shape.top_k,
+        d_ff=shape.d_ff, d_ff_shared=shape.d_ff_shared,
+        router=smr.SOFTMAX_TOPK if shape.router == "softmax" else smr.SIGMOID_GROUP_TOPK,
+        n_group=shape.n_group, topk_group=shape.topk_group,
+        routed_scaling=shape.routed_scaling, renorm_clamp=shape.renorm_clamp,
+        act_dtype=dt[shape.act_dtype], expert_dtype=dt[shape.expert_dtype], path=path)
+
+
+def _uses_tc(shape, T, path):
+    if shape.expert_dtype != "bf16":
+        return False
+    return path == 2 or (path == 0 and T >= TC_MIN_TOKENS)
+
+
 class Workload:
     """Device weight copies, activations and buffers of one token batch."""
 
-    def __init__(self, weights, T, n_copies):
+    def __init__(self, weights, T, n_copies, path):
         import torch
         import moe_inputs as mi
         import sparse_moe_routing_gb300 as smr
         shape, device = weights.shape, weights.device
-        self.shape, self.T, self.device = shape, T, device
+        self.shape, self.T, self.device, self.path = shape, T, device, path
         A = mi.make_activations(shape, T)
         self.host = dict(weights.host)
         self.host.update(A)
         self.copies = weights.get(n_copies)
         self.x = _to_dev(A["x"], device)
         self.r = _to_dev(A["r_attn"], device)
-        self.cfg = smr.MoEConfig(T=T, d_model=shape.d_model, n_experts=shape.n_experts,
-                                 top_k=shape.top_k, d_ff=shape.d_ff,
-                                 d_ff_shared=shape.d_ff_shared,
-                                 routed_scaling=shape.routed_scaling,
-                                 renorm_clamp=shape.renorm_clamp)
+        self.cfg = _cfg(shape, T, path)
         layer = smr.MoELayer(self.cfg, self.copies[0], device)
         self.ws = layer.ws
         self.out = torch.empty((T, shape.d_model), dtype=torch.float32, device=device)
@@ -209,12 +244,12 @@ class Workload:
         w = self.copies[i % len(self.copies)]
         smr.layer_forward(self.cfg, self.ws, self.x, self.r, w["W_router"], w["W_gate"],
                           w["W_up"], w["W_down"], self.out, self.ids, self.wts,
-                          Ws_gate=w["Ws_gate"], Ws_up=w["Ws_up"], Ws_down=w["Ws_down"],
-                          w_shared=w["w_shared"])
+                          expert_bias=w.get("expert_bias"), Ws_gate=w.get("Ws_gate"),
+                          Ws_up=w.get("Ws_up"), Ws_down=w.get("Ws_down"),
+                          w_shared=w.get("w_shared"))
 
 
 def _n_copies(shape, T):
-    import moe_inputs  # noqa: F401
     E, k = shape.n_experts, shape.top_k
     a = E * (1 - (1 - k / E) ** T)
     touched = layer_bytes(shape, T, a)
@@ -274,6 +309,7 @@ def time_e2e(wl, K):
     pinned-host x and r_attn go to the device, the layer runs, and out,
     topk_ids and weights come back to pinned host memory."""
     import torch
+    import sparse_moe_routing_gb300 as smr
     xh = wl.x.cpu().pin_memory()
     rh = wl.r.cpu().pin_memory()
     oh = torch.empty(wl.out.shape, dtype=torch.float32).pin_memory()
@@ -281,7 +317,6 @@ def time_e2e(wl, K):
     wh = torch.empty(wl.wts.shape, dtype=torch.float32).pin_memory()
     x = torch.empty_like(wl.x)
     r = torch.empty_like(wl.r)
-    import sparse_moe_routing_gb300 as smr
     layers = [smr.MoELayer(wl.cfg, w, wl.device) for w in wl.copies]
 
     def one(i):
@@ -308,10 +343,7 @@ def time_e2e(wl, K):
     return ms, h2d, d2h
 
 
-def cpu_baseline(wl, budget_s=12.0):
-    """The fp64 oracle as it stands on this host's cores, on a bounded sample
-    of the same workload (successive chunks of tokens of the same batch)."""
-    import oracle as orc
+def _host_cores():
     cores = len(os.sched_getaffinity(0))
     try:
         import threadpoolctl
@@ -320,6 +352,13 @@ def cpu_baseline(wl, budget_s=12.0):
             cores = max(i.get("num_threads", 1) for i in info)
     except Exception:
         pass
+    return cores
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    """The fp64 oracle as it stands on this host's cores, on a bounded sample
+    of the same workload (successive chunks of tokens of the same batch)."""
+    import oracle as orc
     L = wl.host
     done, t0 = 0, time.perf_counter()
     chunk = 4
@@ -329,7 +368,7 @@ def cpu_baseline(wl, budget_s=12.0):
         orc.moe_layer_forward(L, wl.shape, tokens=toks)
         done += len(toks)
     el = time.perf_counter() - t0
-    return {"value": done / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+    return {"value": done / el, "unit": "tokens/s", "cores": _host_cores(), "kind": "oracle",
             "sample": "%d token-rows cycling over the %d-token batch, %d per call "
                       "(fp64 numpy oracle, %.1f s)" % (done, wl.T, chunk, el)}
 
@@ -351,20 +390,24 @@ def run_ours(args):
         from sparse_moe_routing_gb300 import build
         build.build()
     hbm, tflops, peak_src = _peaks()
-    shape = mi.QWEN36
-    K, W, T = args.steps, args.warmup, args.tokens
-
+    preset, T_default, desc = WORKLOADS[args.workload]
+    shape = mi.PRESETS[preset]
+    path = {"auto": smr.PATH_AUTO, "gemv": smr.PATH_GEMV, "tc": smr.PATH_TC}[args.path]
+    K, W = args.steps, args.warmup
+    T = args.tokens or T_default
     weights = Weights(shape, device)
 
     def measure(T, trace):
-        wl = Workload(weights, T, _n_copies(shape, T))
+        wl = Workload(weights, T, _n_copies(shape, T), path)
+        tc = _uses_tc(shape, T, path)
+        kern = ("tc_gateup" if tc else "gemv_gateup") if trace else None
         sampler = ClockSampler(local) if trace else None
-        ms, launches, durs, (t0, t1) = time_graph(wl, K, W, "gemv_gateup" if trace else None,
-                                                  sampler)
+        ms, launches, durs, (t0, t1) = time_graph(wl, K, W, kern, sampler)
         n_act = int(np.unique(wl.ids.cpu().numpy()).size)
-        return wl, ms, launches, durs, n_act, (sampler.summary(t0, t1) if sampler else None)
+        clocks = sampler.summary(t0, t1) if sampler else None
+        return wl, ms, launches, durs, n_act, clocks, kern
 
-    wl, ms, launches, durs, n_act, clocks = measure(T, True)
+    wl, ms, launches, durs, n_act, clocks, kern = measure(T, True)
     t_max = torch.tensor([ms], device=device)
     if world > 1:
         torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
@@ -372,48 +415,65 @@ def run_ours(args):
     ms_step = ms / K
     value = world * T * K / (ms / 1e3)
 
+    # roofline of the dominant kernel: bytes and flops per launch, bound by
+    # whichever floor is larger
     mean_k = sum(durs) / len(durs) if durs else None
-    ach = gateup_bytes(shape, T, n_act) / (mean_k * 1e-3) / 1e9 if mean_k else None
-    tr = _traffic("gemv_gateup")
-    roofline = {"kernel": "gemv_gateup (routed + shared gate/up + SwiGLU)", "bound": "hbm",
-                "achieved": ach, "peak": hbm, "unit": "GB/s",
-                "frac": ach / hbm if ach else None,
-                "traffic": (tr["dram_bytes_per_unit"] * (n_act + 1) if tr else None),
-                "peak_source": peak_src,
-                "algorithmic_bytes_per_launch": gateup_bytes(shape, T, n_act),
-                "units_per_launch": n_act + 1, "mean_launch_us": mean_k * 1e3 if mean_k else None}
-    lb = layer_bytes(shape, T, n_act)
-    config = {"workload": "qwen3.6-35b-a3b moe layer forward, decode batch T=%d" % T,
-              "T": T, "d_model": shape.d_model, "n_experts": shape.n_experts,
-              "top_k": shape.top_k, "d_ff": shape.d_ff, "d_ff_shared": shape.d_ff_shared,
-              "router": "softmax top-8, renorm clamp 2^-14", "weights": "bf16, fp32 accumulate",
+    gb, gf = gateup_work(shape, T, n_act)
+    hbm_bound = gb / (hbm * 1e9) >= gf / (tflops * 1e12)
+    if mean_k:
+        sec = mean_k * 1e-3
+        ach = gb / sec / 1e9 if hbm_bound else gf / sec / 1e12
+    else:
+        ach = None
+    peak = hbm if hbm_bound else tflops
+    tr = _traffic(kern)
+    roofline = {"kernel": kern + " (routed + shared gate/up + SwiGLU)",
+                "bound": "hbm" if hbm_bound else "tensor", "achieved": ach, "peak": peak,
+                "unit": "GB/s" if hbm_bound else "TFLOP/s",
+                "frac": ach / peak if ach else None,
+                "traffic": (tr["dram_bytes_per_unit"] * (n_act + (1 if shape.d_ff_shared else 0))
+                            if tr else None),
+                "peak_source": peak_src, "algorithmic_bytes_per_launch": gb,
+                "algorithmic_flops_per_launch": gf,
+                "units_per_launch": n_act + (1 if shape.d_ff_shared else 0),
+                "mean_launch_us": mean_k * 1e3 if mean_k else None}
+    lb, lf = layer_bytes(shape, T, n_act), layer_flops(shape, T)
+    config = {"workload": desc % T, "T": T, "d_model": shape.d_model,
+              "n_experts": shape.n_experts, "top_k": shape.top_k, "d_ff": shape.d_ff,
+              "d_ff_shared": shape.d_ff_shared, "router": shape.router,
+              "weights": "%s, fp32 accumulate" % shape.expert_dtype,
+              "expert_path": "tcgen05 grouped GEMM" if _uses_tc(shape, T, path)
+              else "CUDA-core streaming GEMV",
               "l2": "weights rotate over %d distinct layer copies (>= 4x L2 per pass)"
                     % len(wl.copies),
               "timing": "one CUDA graph of K steps, replayed once; CUDA events",
               "parallelism": "replicas" if world == 1 else "dp%d (independent replicas)" % world,
-              "active_experts": n_act,
-              "layer_alg_bytes": lb, "layer_hbm_frac": lb / (ms_step * 1e-3) / 1e9 / hbm}
-    sweep = {}
-    if not args.no_sweep:
+              "active_experts": n_act, "layer_alg_bytes": lb, "layer_alg_flops": lf,
+              "layer_hbm_frac": lb / (ms_step * 1e-3) / 1e9 / hbm,
+              "layer_tensor_frac": lf / (ms_step * 1e-3) / 1e12 / tflops}
+    if not args.no_sweep and args.workload == "decode":
+        sweep = {}
         for Ts in (1, 8, 64):
             if Ts == T:
                 sweep[str(Ts)] = {"tokens_per_s": T * K / (ms / 1e3), "ms_per_step": ms_step,
                                   "layer_hbm_frac": config["layer_hbm_frac"]}
                 continue
-            wls, mss, _, _, na, _ = measure(Ts, False)
+            wls, mss, _, _, na, _, _ = measure(Ts, False)
             b = layer_bytes(shape, Ts, na)
             sweep[str(Ts)] = {"tokens_per_s": Ts * K / (mss / 1e3), "ms_per_step": mss / K,
                               "active_experts": na,
                               "layer_hbm_frac": b / (mss / K * 1e-3) / 1e9 / hbm}
             del wls
         config["sweep"] = sweep
-    e2e_ms, h2d, d2h = time_e2e(wl, min(K, 200))
-    e2e = {"value": world * T * min(K, 200) / (e2e_ms / 1e3), "unit": "tokens/s",
+    k_e2e = min(K, 200)
+    e2e_ms, h2d, d2h = time_e2e(wl, k_e2e)
+    e2e = {"value": world * T * k_e2e / (e2e_ms / 1e3), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
-            "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clocks}
+            "vs_baseline": None, "dtype": shape.expert_dtype, "data": "synthetic",
+            "config": config, "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
@@ -431,9 +491,10 @@ def run_reference(args):
         return
     import moe_inputs as mi
     import oracle as orc
-    shape, T = mi.QWEN36, args.tokens
+    preset, T_default, desc = WORKLOADS[args.workload]
+    shape = mi.PRESETS[preset]
+    T = args.tokens or T_default
     L = mi.make_layer(shape, T)
-    cores = len(os.sched_getaffinity(0))
     t0 = time.perf_counter()
     orc.moe_layer_forward(L, shape, tokens=[0])
     t_tok = time.perf_counter() - t0
@@ -459,10 +520,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
         "steps": K, "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "qwen3.6-35b-a3b moe layer forward, decode batch T=%d" % T,
-                   "T": T},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+        "config": {"workload": desc % T, "T": T},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _host_cores(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0}}))
 
@@ -472,7 +532,9 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--tokens", type=int, default=64)
+    ap.add_argument("--tokens", type=int, default=0, help="token batch (default: workload's)")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    ap.add_argument("--path", choices=["auto", "gemv", "tc"], default="auto")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

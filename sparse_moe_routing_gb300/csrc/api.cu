@@ -24,7 +24,7 @@ struct Plan {
 
 // Token batches at or above this size take the tensor-core path under
 // MOE_PATH_AUTO (when the shape allows it).
-constexpr int kTcMinTokens = 16;
+constexpr int kTcMinTokens = 4;
 
 // The tensor-core path: bf16 experts and activations, K dims multiples of the
 // 64-element TMA box, N tiles of 128 (gate/up) and 256 (down), and a shared
