@@ -20,7 +20,7 @@ events inside the graph (moe_trace_kernel) for the roofline figure.
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--tokens T]
                        [--workload decode|prefill|deepseek|mixtral]
                        [--path auto|gemv|tc] [--impl ours|reference]
-                       [--no-sweep] [--no-cpu-baseline]
+                       [--no-sweep] [--no-cpu-baseline] [--breakdown]
 For N > 1 launch with torchrun (one rank per GPU, NCCL): every rank runs an
 independent replica on its own token batch (the layer has no cross-token
 exchange), so the job processes N*T tokens per step ("scaling": "weak").
@@ -465,6 +465,16 @@ def run_ours(args):
                               "layer_hbm_frac": b / (mss / K * 1e-3) / 1e9 / hbm}
             del wls
         config["sweep"] = sweep
+    if args.breakdown:
+        # one more graph replay per kernel family, that family bracketed by
+        # events: mean in-graph duration per launch (us)
+        bd = {}
+        kb = min(K, 50)
+        for fam in smr.KERNELS:
+            durs_f = time_graph(wl, kb, 3, fam)[2]
+            if durs_f:
+                bd[fam] = round(sum(durs_f) / len(durs_f) * 1e3, 2)
+        config["breakdown_us"] = bd
     k_e2e = min(K, 200)
     e2e_ms, h2d, d2h = time_e2e(wl, k_e2e)
     e2e = {"value": world * T * k_e2e / (e2e_ms / 1e3), "unit": "tokens/s",
@@ -538,6 +548,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--breakdown", action="store_true",
+                    help="also report the mean in-graph time of every kernel family")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

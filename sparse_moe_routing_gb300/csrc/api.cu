@@ -34,6 +34,21 @@ bool tc_shape_ok(const moe_cfg_t& c) {
          c.d_ff % 128 == 0 && (c.d_ff_shared == 0 || c.d_ff_shared == c.d_ff);
 }
 
+// The router contraction on the tensor cores: bf16, E a multiple of 32 (N
+// tiles of 32 or 64 logits), d a multiple of the 64-element box, and enough
+// tokens to fill 128-row tiles usefully (below this the CUDA-core router is
+// as fast, measured at T=64, and needs no separate shared-gate launch).
+constexpr int kTcRouterMinTokens = 128;
+bool use_tc_router(const moe_cfg_t& c) {
+  return c.act_dtype == MOE_BF16 && c.n_experts % 32 == 0 && c.n_experts <= 512 &&
+         c.d_model % 64 == 0 && c.T >= kTcRouterMinTokens;
+}
+// N tile of the tensor-core router: 32 logits for small batches (more CTAs
+// share the router weights), 64 for large ones.
+int tc_router_bn(const moe_cfg_t& c) {
+  return (c.T <= 1024 || c.n_experts % 64 != 0) ? 32 : 64;
+}
+
 bool use_tc(const moe_cfg_t& c) {
   if (!tc_shape_ok(c)) return false;
   if (c.path == MOE_PATH_TC) return true;
@@ -193,9 +208,39 @@ moe_status_t enqueue_route(const void* x, const void* W_router, const float* bia
   ta.routed_scaling = c->routed_scaling;
   ta.renorm_clamp = c->renorm_clamp;
   const bool bf16 = c->act_dtype == MOE_BF16;
-  cudaError_t e = run(MOE_KERNEL_ROUTER_LOGITS, st,
-                      [&] { return launch_router_logits(ra, bf16, st); });
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e;
+  if (use_tc_router(*c)) {
+    // tensor-core router: logits [T][E] (column E unused), then the shared
+    // gate from its own warp-per-token dot product
+    const int bn = tc_router_bn(*c);
+    TcMaps m{};
+    if (!tc_make_map(&m.A0, x, c->T, c->d_model, 128) ||
+        !tc_make_map(&m.B0, W_router, c->n_experts, c->d_model, bn))
+      return MOE_ERR_CUDA;
+    m.A1 = m.A0;
+    m.B1 = m.B2 = m.B3 = m.B0;
+    TcArgs a{};
+    a.out_routed = ra.logits;
+    a.ctrl = at<Ctrl>(c, 0);
+    a.E = c->n_experts;
+    a.T = c->T;
+    a.K = c->d_model;
+    a.ld_out = c->n_experts + 1;
+    a.bn = bn;
+    a.n_tiles = c->n_experts / bn;
+    const int items = (c->T + kTcBm - 1) / kTcBm * a.n_tiles;
+    e = run(MOE_KERNEL_TC_ROUTER, st, [&] { return launch_tc_gemm(kTcRouter, m, a, items, st); });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    ta.has_shared_logit = 0;
+    if (s_shared) {
+      RouterArgs rs{x, nullptr, w_shared, ra.logits, c->T, c->d_model, 0};
+      e = run(MOE_KERNEL_SHARED_GATE, st, [&] { return launch_shared_gate(rs, s_shared, bf16, st); });
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+  } else {
+    e = run(MOE_KERNEL_ROUTER_LOGITS, st, [&] { return launch_router_logits(ra, bf16, st); });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
   return cuda_status(run(MOE_KERNEL_ROUTER_TOPK, st, [&] { return launch_router_topk(ta, st); }));
 }
 
@@ -384,7 +429,7 @@ moe_status_t moe_trace_kernel(int kernel, void* const* starts, void* const* stop
     g_trace = TraceState{};
     return MOE_OK;
   }
-  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_GATHER || n <= 0 || !starts ||
+  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_TC_ROUTER || n <= 0 || !starts ||
       !stops || !count)
     return MOE_ERR_INVALID_ARG;
   g_trace.kernel = kernel;

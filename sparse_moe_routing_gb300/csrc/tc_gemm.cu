@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        float* out = static_cast<float*>(a.out_routed) + (size_t)i * a.ld_out;
+        float* out = static_cast<float*>(a.out_routed) + (size_t)i * a.ld_out + ti.nt * a.bn;
         for (int c0 = 0; c0 < a.bn; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(tbase + c0, v);

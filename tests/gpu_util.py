@@ -121,9 +121,14 @@ def check_routing(gpu_ids: np.ndarray, gpu_w: np.ndarray, ref: dict, shape, rows
         wref = dict(zip(want, ref["weights"][r]))
         if min(kgap, ggap) > GAP:
             assert sorted(got) == sorted(want), (t, got, want, kgap)
-            for s in range(k - 1):
-                if cand[want[s]] - cand[want[s + 1]] > GAP:
-                    assert got[s] == want[s], (t, s, got, want)
+            # slot order: the oracle's slots split into runs of near-equal
+            # scores (neighbour gap <= GAP); each run must hold the same ids,
+            # in any order (equal keys have no unique order)
+            start = 0
+            for s in range(k):
+                if s == k - 1 or cand[want[s]] - cand[want[s + 1]] > GAP:
+                    assert sorted(got[start:s + 1]) == sorted(want[start:s + 1]), (t, got, want)
+                    start = s + 1
         else:
             near += 1
             if sorted(got) != sorted(want):
