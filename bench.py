@@ -52,6 +52,8 @@ WORKLOADS = {
                 "qwen3.6-35b-a3b moe layer forward, prefill T=%d, skewed routing"),
     "deepseek": ("deepseek_group", 4096, "deepseek-style sigmoid group top-k layer, T=%d"),
     "mixtral": ("mixtral_bf16", 2048, "mixtral-style top-2 layer, bf16, T=%d"),
+    "mixtral_q4": ("mixtral_q4", 2048,
+                   "mixtral-style top-2 layer, 4-bit affine g64 experts, T=%d"),
 }
 
 
@@ -68,16 +70,22 @@ def _peaks():
 # algorithmic work (what the layer must move / compute; intermediates excluded)
 # ----------------------------------------------------------------------------
 def _wbytes(shape):
-    return 2 if shape.expert_dtype == "bf16" else 4
+    """Bytes per routed-expert weight: bf16 2, f32 4, 4-bit affine g64 0.5 plus
+    a bf16 scale and min per 64 weights (0.5625)."""
+    return {"bf16": 2, "f32": 4, "q4": 0.5 + 4 / 64}[shape.expert_dtype]
+
+
+def _abytes(shape):
+    return 2 if shape.act_dtype == "bf16" else 4
 
 
 def layer_bytes(shape, T, n_active):
     d, E, I, Is, k = shape.d_model, shape.n_experts, shape.d_ff, shape.d_ff_shared, shape.top_k
-    wb = _wbytes(shape)
-    b = E * d * wb + (d * wb if Is else 0)                 # router (+ shared gate)
-    b += n_active * 3 * I * d * wb + 3 * Is * d * wb       # active experts + shared expert
-    b += T * d * wb + 2 * T * d * 4 + T * k * 8            # x, r_attn, out, ids+weights
-    return b
+    wb, ab = _wbytes(shape), _abytes(shape)
+    b = E * d * ab + (d * ab if Is else 0)                 # router (+ shared gate)
+    b += n_active * 3 * I * d * wb + 3 * Is * d * ab       # active experts + shared expert
+    b += T * d * ab + 2 * T * d * 4 + T * k * 8            # x, r_attn, out, ids+weights
+    return int(b)
 
 
 def layer_flops(shape, T):
@@ -91,10 +99,10 @@ def gateup_work(shape, T, n_active):
     shape) plus the activations x; flops 2*d*2*I per routed pair and per
     shared row."""
     d, I, Is, k = shape.d_model, shape.d_ff, shape.d_ff_shared, shape.top_k
-    wb = _wbytes(shape)
-    b = n_active * 2 * I * d * wb + 2 * Is * d * wb + T * d * wb
+    wb, ab = _wbytes(shape), _abytes(shape)
+    b = n_active * 2 * I * d * wb + 2 * Is * d * ab + T * d * ab
     f = 2 * T * k * d * 2 * I + 2 * T * d * 2 * Is
-    return b, f
+    return int(b), f
 
 
 # ----------------------------------------------------------------------------
@@ -212,6 +220,8 @@ def _cfg(shape, T, path):
 
 
 def _uses_tc(shape, T, path):
+    if shape.expert_dtype == "q4":
+        return True  # 4-bit banks are dequantised inside the tensor-core kernel
     if shape.expert_dtype != "bf16":
         return False
     return path == 2 or (path == 0 and T >= TC_MIN_TOKENS)
@@ -242,11 +252,16 @@ class Workload:
     def step(self, i):
         import sparse_moe_routing_gb300 as smr
         w = self.copies[i % len(self.copies)]
-        smr.layer_forward(self.cfg, self.ws, self.x, self.r, w["W_router"], w["W_gate"],
-                          w["W_up"], w["W_down"], self.out, self.ids, self.wts,
+        smr.layer_forward(self.cfg, self.ws, self.x, self.r, w["W_router"], _bank(w, "W_gate"),
+                          _bank(w, "W_up"), _bank(w, "W_down"), self.out, self.ids, self.wts,
                           expert_bias=w.get("expert_bias"), Ws_gate=w.get("Ws_gate"),
                           Ws_up=w.get("Ws_up"), Ws_down=w.get("Ws_down"),
                           w_shared=w.get("w_shared"))
+
+
+def _bank(w, name):
+    """A bank tensor, or the (codes, scale, min) tuple of a 4-bit bank."""
+    return w[name] if name in w else (w[name + "_q"], w[name + "_scale"], w[name + "_min"])
 
 
 def _n_copies(shape, T):

@@ -290,8 +290,11 @@ class MoELayer:
     def forward(self, x, r_attn, out=None, stream=None):
         w = self.w
         out = self.out if out is None else out
-        layer_forward(self.cfg, self.ws, x, r_attn, w["W_router"], w["W_gate"], w["W_up"],
-                      w["W_down"], out, self.ids, self.weights,
+        def bank(name):  # a tensor, or the (codes, scale, min) of a 4-bit bank
+            return w[name] if name in w else (w[name + "_q"], w[name + "_scale"], w[name + "_min"])
+
+        layer_forward(self.cfg, self.ws, x, r_attn, w["W_router"], bank("W_gate"), bank("W_up"),
+                      bank("W_down"), out, self.ids, self.weights,
                       expert_bias=w.get("expert_bias"), Ws_gate=w.get("Ws_gate"),
                       Ws_up=w.get("Ws_up"), Ws_down=w.get("Ws_down"),
                       w_shared=w.get("w_shared"), stream=stream)

@@ -29,9 +29,12 @@ constexpr int kTcMinTokens = 4;
 // The tensor-core path: bf16 experts and activations, K dims multiples of the
 // 64-element TMA box, N tiles of 128 (gate/up) and 256 (down), and a shared
 // expert (if any) as wide as the routed ones.
+// 4-bit affine banks are dequantised inside this path (one 64-code group per
+// 64-element k-block); they are supported without a shared expert only.
 bool tc_shape_ok(const moe_cfg_t& c) {
-  return c.expert_dtype == MOE_BF16 && c.act_dtype == MOE_BF16 && c.d_model % 256 == 0 &&
-         c.d_ff % 128 == 0 && (c.d_ff_shared == 0 || c.d_ff_shared == c.d_ff);
+  if (c.act_dtype != MOE_BF16 || c.d_model % 256 != 0 || c.d_ff % 128 != 0) return false;
+  if (c.expert_dtype == MOE_Q4_AFFINE_G64) return c.d_ff_shared == 0;
+  return c.expert_dtype == MOE_BF16 && (c.d_ff_shared == 0 || c.d_ff_shared == c.d_ff);
 }
 
 // The router contraction on the tensor cores: bf16, E a multiple of 32 (N
@@ -51,7 +54,7 @@ int tc_router_bn(const moe_cfg_t& c) {
 
 bool use_tc(const moe_cfg_t& c) {
   if (!tc_shape_ok(c)) return false;
-  if (c.path == MOE_PATH_TC) return true;
+  if (c.path == MOE_PATH_TC || c.expert_dtype == MOE_Q4_AFFINE_G64) return true;
   return c.path == MOE_PATH_AUTO && c.T >= kTcMinTokens;
 }
 
@@ -113,8 +116,9 @@ moe_status_t validate_cfg(const moe_cfg_t* c) {
   if (c->expert_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (!gemv_supported(c->d_model, c->d_ff > c->d_ff_shared ? c->d_ff : c->d_ff_shared))
     return MOE_ERR_UNSUPPORTED;
-  if (c->expert_dtype == MOE_Q4_AFFINE_G64) return MOE_ERR_UNSUPPORTED;  // not built yet
-  if (c->path == MOE_PATH_TC && !tc_shape_ok(*c)) return MOE_ERR_UNSUPPORTED;
+  if ((c->path == MOE_PATH_TC || c->expert_dtype == MOE_Q4_AFFINE_G64) && !tc_shape_ok(*c))
+    return MOE_ERR_UNSUPPORTED;
+  if (c->expert_dtype == MOE_Q4_AFFINE_G64 && c->path == MOE_PATH_GEMV) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -305,11 +309,23 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
   a.E = E;
   a.T = T;
 
-  // gate/up: A = X_perm (routed) / x (shared), B = gate and up rows
+  const bool q4 = c->expert_dtype == MOE_Q4_AFFINE_G64;
+  auto bmap = [&](CUtensorMap* mp, const void* w, uint64_t rows, uint64_t K, uint32_t box) {
+    return q4 ? tc_make_map_q4(mp, w, rows, K, box) : tc_make_map(mp, w, rows, K, box);
+  };
+  // gate/up: A = X_perm (routed) / x (shared), B = gate and up rows (4-bit
+  // codes for q4 banks, dequantised in the kernel)
   TcMaps m{};
   bool ok = tc_make_map(&m.A0, xperm, P, d, 128) && tc_make_map(&m.A1, x, T, d, 128) &&
-            tc_make_map(&m.B0, Wg.w, (uint64_t)E * I, d, 128) &&
-            tc_make_map(&m.B1, Wu.w, (uint64_t)E * I, d, 128);
+            bmap(&m.B0, Wg.w, (uint64_t)E * I, d, 128) &&
+            bmap(&m.B1, Wu.w, (uint64_t)E * I, d, 128);
+  if (q4) {
+    a.qs0 = static_cast<const __nv_bfloat16*>(Wg.scale);
+    a.qm0 = static_cast<const __nv_bfloat16*>(Wg.minv);
+    a.qs1 = static_cast<const __nv_bfloat16*>(Wu.scale);
+    a.qm1 = static_cast<const __nv_bfloat16*>(Wu.minv);
+    a.qgroups = d / 64;
+  }
   if (ok && shared) ok = tc_make_map(&m.B2, Wsg, Is, d, 128) && tc_make_map(&m.B3, Wsu, Is, d, 128);
   if (!ok) return MOE_ERR_CUDA;
   if (!shared) {
@@ -329,7 +345,13 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
 
   // down: A = H (routed) / Hs (shared), B = down rows; alpha in the epilogue
   TcMaps m2{};
-  ok = tc_make_map(&m2.A0, H, P, I, 128) && tc_make_map(&m2.B0, Wd.w, (uint64_t)E * d, I, 256);
+  ok = tc_make_map(&m2.A0, H, P, I, 128) && bmap(&m2.B0, Wd.w, (uint64_t)E * d, I, 256);
+  if (q4) {
+    a.qs0 = static_cast<const __nv_bfloat16*>(Wd.scale);
+    a.qm0 = static_cast<const __nv_bfloat16*>(Wd.minv);
+    a.qs1 = a.qm1 = nullptr;
+    a.qgroups = I / 64;
+  }
   if (ok && shared) ok = tc_make_map(&m2.A1, Hs, T, Is, 128) && tc_make_map(&m2.B2, Wsd, d, Is, 256);
   if (!ok) return MOE_ERR_CUDA;
   if (!shared) {

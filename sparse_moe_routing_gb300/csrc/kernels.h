@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -97,6 +98,13 @@ struct TcArgs {
   int n_tiles;                 // N tiles per row block
   int bn;                      // N of one MMA (gate/up: 128 gate + 128 up)
   int brows_routed;            // rows of one routed expert in the 2D B view
+  // 4-bit affine weights (null for bf16): per-row group scale and min, bf16
+  // [rows][K/64]; 0 = gate (or down), 1 = up
+  const __nv_bfloat16* qs0;
+  const __nv_bfloat16* qm0;
+  const __nv_bfloat16* qs1;
+  const __nv_bfloat16* qm1;
+  int qgroups;                 // K / 64
 };
 
 // The six operand maps: A routed/shared, B0/B1 routed, B2/B3 shared.
@@ -108,6 +116,9 @@ struct TcMaps {
 // 128-byte swizzle; false if the driver entry point or the encoding fails.
 bool tc_make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);
+// Encodes a 2D uint8 TMA map of 4-bit codes [rows][K/2], box 32 B x box_rows.
+bool tc_make_map_q4(CUtensorMap* m, const void* codes, uint64_t rows, uint64_t K,
+                    uint32_t box_rows);
 cudaError_t launch_tc_gemm(int mode, const TcMaps& maps, const TcArgs& a, int max_items,
                            cudaStream_t st);
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int d, void* out, int P,

@@ -29,12 +29,12 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BK = 64, STAGES = 4;
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 epilogue
+// Warp roles: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 2-5
+// epilogue, and (4-bit weights only) warps 6-9 dequantise the B stages.
+constexpr int BM = 128, BK = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStageA = BM * BK * 2;      // 16 KB
 constexpr int kStageB = 256 * BK * 2;     // 32 KB (largest B tile)
-constexpr size_t kSmemBytes = 1024 + STAGES * (kStageA + kStageB) + 256;
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -132,6 +132,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void st_shared_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(p)), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
@@ -176,20 +182,86 @@ __device__ __forceinline__ void give_up(const TcArgs& a, volatile int* abort_fla
   report(a.ctrl, kDevTimeout, site);
 }
 
+// Shared-memory plan of one CTA (1024-byte aligned stages).
+template <bool Q4>
+struct SmemPlan {
+  static constexpr int kStages = Q4 ? 3 : 4;
+  static constexpr int kStageQ = 256 * (BK / 2);  // raw 4-bit codes of one B stage
+  static constexpr int kThreadsCta = Q4 ? 320 : 192;
+  static constexpr size_t kA = 0;
+  static constexpr size_t kB = kA + (size_t)kStages * kStageA;
+  static constexpr size_t kQ = kB + (size_t)kStages * kStageB;
+  static constexpr size_t kBars = kQ + (Q4 ? (size_t)kStages * kStageQ : 0);
+  static constexpr size_t kBytes = 1024 + kBars + 256;
+};
+
+// Dequantises one B stage: 256 rows x 64 codes (4-bit affine, one group per
+// row per stage) from the raw ring into bf16 in the 128-byte-swizzled K-major
+// layout that TMA would have produced for a bf16 tile. Thread `tid` (of 128)
+// handles rows tid and tid + 128.
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void dequant_stage(const TcArgs& a, const TileInfo& ti, int kb,
+                                              const uint8_t* q_stage, uint8_t* b_stage, int tid) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = tid + 128 * h;
+    // global row of this B row in its bank, and its (scale, min) arrays
+    const __nv_bfloat16* qs;
+    const __nv_bfloat16* qm;
+    size_t grow;
+    if (MODE == kTcGateUp) {
+      const int rr = r & 127;
+      grow = (size_t)ti.g * a.brows_routed + (size_t)ti.nt * 128 + rr;
+      qs = r < 128 ? a.qs0 : a.qs1;
+      qm = r < 128 ? a.qm0 : a.qm1;
+    } else {
+      grow = (size_t)ti.g * a.brows_routed + (size_t)ti.nt * 256 + r;
+      qs = a.qs0;
+      qm = a.qm0;
+    }
+    const size_t gi = grow * a.qgroups + kb;
+    const float scale = __bfloat162float(qs[gi]);
+    const float mn = __bfloat162float(qm[gi]);
+    const uint4 c0 = reinterpret_cast<const uint4*>(q_stage + r * 32)[0];
+    const uint4 c1 = reinterpret_cast<const uint4*>(q_stage + r * 32)[1];
+    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    uint8_t* row_base = b_stage + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      // word c holds elements 8c..8c+7, the even element in the low nibble
+      const uint32_t w = words[c];
+      uint32_t packed[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t byte = (w >> (8 * b)) & 0xFFu;
+        // exact small-integer to float: 2^23 + q has q in its low mantissa bits
+        const float q0 = __uint_as_float(0x4B000000u | (byte & 0xFu)) - 8388608.0f;
+        const float q1 = __uint_as_float(0x4B000000u | (byte >> 4)) - 8388608.0f;
+        packed[b] = pack_bf16x2(fmaf(scale, q0, mn), fmaf(scale, q1, mn));
+      }
+      st_shared_v4(row_base + ((c ^ (r & 7)) << 4), packed[0], packed[1], packed[2], packed[3]);
+    }
+  }
+}
+
+template <int MODE, bool Q4>
+__global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmB3,
                    const TcArgs a) {
+  using SP = SmemPlan<Q4>;
+  constexpr int STAGES = SP::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * kStageA;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * kStageB);
+  uint8_t* sA = smem + SP::kA;
+  uint8_t* sB = smem + SP::kB;
+  uint8_t* sQ = smem + SP::kQ;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SP::kBars);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint64_t* rawfull = empty + STAGES;   // Q4 only: A tile + raw codes landed
+  uint64_t* tfull = rawfull + STAGES;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -198,8 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int site = MODE == kTcGateUp ? kSiteTcGateUp : (MODE == kTcDown ? kSiteTcDown : kSiteTcRouter);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], Q4 ? 4 : 1);  // Q4: one arrival per dequant warp
       mbar_init(&empty[s], 1);
+      mbar_init(&rawfull[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -228,7 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // MMAs. A wait's outcome is lane 0's, broadcast to the warp.
   if (warp == 0) {
     // -------------------------------------------------------------- producer
-    const uint32_t stage_bytes = kStageA + a.bn * BK * 2;
+    // bf16 B: A + B tiles land on full[]. Q4 B: A + raw code tiles land on
+    // rawfull[] and the dequant warps then fill the B stage.
+    const uint32_t stage_bytes =
+        Q4 ? kStageA + a.bn * (BK / 2) : kStageA + a.bn * BK * 2;
     int stage = 0;
     uint32_t ph = 0;
     bool alive = true;
@@ -250,12 +326,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (lane == 0) {
-          mbar_expect_tx(&full[stage], stage_bytes);
-          uint8_t* b_dst = sB + stage * kStageB;
-          tma_load_2d(sA + stage * kStageA, mA, &full[stage], kb * BK, arow);
-          tma_load_2d(b_dst, mB0, &full[stage], kb * BK, brow);
-          if (MODE == kTcGateUp)
-            tma_load_2d(b_dst + bhalf * BK * 2, mB1, &full[stage], kb * BK, brow);
+          uint64_t* bar = Q4 ? &rawfull[stage] : &full[stage];
+          mbar_expect_tx(bar, stage_bytes);
+          tma_load_2d(sA + stage * kStageA, mA, bar, kb * BK, arow);
+          if (Q4) {
+            uint8_t* q_dst = sQ + stage * SP::kStageQ;
+            tma_load_2d(q_dst, mB0, bar, kb * (BK / 2), brow);
+            if (MODE == kTcGateUp)
+              tma_load_2d(q_dst + bhalf * (BK / 2), mB1, bar, kb * (BK / 2), brow);
+          } else {
+            uint8_t* b_dst = sB + stage * kStageB;
+            tma_load_2d(b_dst, mB0, bar, kb * BK, brow);
+            if (MODE == kTcGateUp)
+              tma_load_2d(b_dst + bhalf * BK * 2, mB1, bar, kb * BK, brow);
+          }
         }
         __syncwarp();
         if (++stage == STAGES) {
@@ -280,7 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
       for (int kb = 0; kb < nkb; ++kb) {
-        ok = lane == 0 ? mbar_wait(&full[stage], ph) : true;
+        ok = true;
+        if (lane == 0) {
+          ok = mbar_wait(&full[stage], ph);
+          if (Q4 && ok) ok = mbar_wait(&rawfull[stage], ph);  // the A tile of this stage
+        }
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
         if (!ok) {
           if (lane == 0) give_up(a, abort_flag, site);
@@ -310,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
-  } else {
+  } else if (warp < 6) {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;
@@ -388,6 +476,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
+  } else if (Q4) {
+    // --------------------------------------------------------------- dequant
+    // Warps 6-9 follow the producer's (tile, k-block) order: wait for the raw
+    // stage, write the bf16 B stage, make the generic-proxy writes visible to
+    // the tensor core's async proxy, then arrive on full[] (one per warp).
+    const int tid = threadIdx.x - 192;
+    int stage = 0;
+    uint32_t ph = 0;
+    bool alive = true;
+    for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
+      const TileInfo ti = decode_tile<MODE>(a, t);
+      for (int kb = 0; kb < nkb; ++kb) {
+        bool ok = lane == 0 ? mbar_wait(&rawfull[stage], ph) : true;
+        ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
+        if (!ok) {
+          if (lane == 0) give_up(a, abort_flag, site);
+          alive = false;
+          break;
+        }
+        dequant_stage<MODE>(a, ti, kb, sQ + stage * SP::kStageQ, sB + stage * kStageB, tid);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -464,17 +581,33 @@ int tc_sm_count() {
 
 namespace {
 
-template <int MODE>
+template <int MODE, bool Q4>
 cudaError_t launch_tc(const TcMaps& maps, const TcArgs& a, int max_items, cudaStream_t st) {
+  using SP = SmemPlan<Q4>;
   static int attr[64] = {};
-  cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE>, (int)kSmemBytes, attr);
+  cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE, Q4>, (int)SP::kBytes, attr);
   if (e != cudaSuccess) return e;
   int grid = tc_sm_count();
   if (max_items < grid) grid = max_items;
   if (grid < 1) grid = 1;
-  tc_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, st>>>(maps.A0, maps.A1, maps.B0, maps.B1,
-                                                           maps.B2, maps.B3, a);
+  tc_gemm_kernel<MODE, Q4><<<grid, SP::kThreadsCta, SP::kBytes, st>>>(
+      maps.A0, maps.A1, maps.B0, maps.B1, maps.B2, maps.B3, a);
   return cudaGetLastError();
+}
+
+// 2D uint8 view of 4-bit codes [rows][K/2 bytes], box = 32 bytes (one 64-code
+// group) x box_rows rows, no swizzle.
+bool make_map_q4(CUtensorMap* m, const void* codes, uint64_t rows, uint64_t K, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || !codes) return false;
+  if (rows == 0) rows = 1;
+  cuuint64_t dims[2] = {K / 2, rows};
+  cuuint64_t strides[1] = {K / 2};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -484,11 +617,21 @@ bool tc_make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
   return make_map(m, base, rows, cols, box_rows);
 }
 
+bool tc_make_map_q4(CUtensorMap* m, const void* codes, uint64_t rows, uint64_t K,
+                    uint32_t box_rows) {
+  return make_map_q4(m, codes, rows, K, box_rows);
+}
+
 cudaError_t launch_tc_gemm(int mode, const TcMaps& maps, const TcArgs& a, int max_items,
                            cudaStream_t st) {
-  if (mode == kTcGateUp) return launch_tc<kTcGateUp>(maps, a, max_items, st);
-  if (mode == kTcDown) return launch_tc<kTcDown>(maps, a, max_items, st);
-  return launch_tc<kTcRouter>(maps, a, max_items, st);
+  if (a.qs0) {
+    if (mode == kTcGateUp) return launch_tc<kTcGateUp, true>(maps, a, max_items, st);
+    if (mode == kTcDown) return launch_tc<kTcDown, true>(maps, a, max_items, st);
+    return cudaErrorInvalidValue;
+  }
+  if (mode == kTcGateUp) return launch_tc<kTcGateUp, false>(maps, a, max_items, st);
+  if (mode == kTcDown) return launch_tc<kTcDown, false>(maps, a, max_items, st);
+  return launch_tc<kTcRouter, false>(maps, a, max_items, st);
 }
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int d, void* out, int P,

@@ -284,3 +284,44 @@ def test_both_expert_paths_match_oracle(shape, T, path):
     print("%s T=%d path=%d out_err=%.3e y_moe_err=%.3e" % (shape.name, T, path, err, y_err))
     assert err <= OUT_TOL[shape.act_dtype]
     assert y_err <= 10 * OUT_TOL[shape.act_dtype]
+
+
+# 4-bit affine group-64 experts (dequantised inside the tensor-core kernel):
+# a small full-oracle shape and the Mixtral-style layer at T=2048.
+Q4_SMALL = mi.MoEShape("q4_small", 8, d_model=512, n_experts=4, top_k=2, d_ff=256,
+                       d_ff_shared=0, expert_dtype="q4", tokens=(300,))
+Q4_CASES = [(Q4_SMALL, 300, 300), (Q4_SMALL, 37, 37), (Q4_SMALL, 1, 1), (mi.MIXTRAL_Q4, 2048, 6)]
+
+
+@pytest.mark.parametrize("shape,T,n_check", Q4_CASES,
+                         ids=["%s-T%d" % (c[0].name, c[1]) for c in Q4_CASES])
+def test_q4_layer_forward_parity(shape, T, n_check):
+    L, dev, cfg, ws = _run_layer(shape, T)
+    ids = dev.ids.cpu().numpy()
+    ref_r = _oracle_routing(L, shape)
+    near = check_routing(ids, dev.w.cpu().numpy(), ref_r, shape)
+    rows = _sample(T, n_check, seed=5)
+    ref = orc.moe_layer_forward(L, shape, tokens=rows)
+    agree = [i for i, t in enumerate(rows) if sorted(ids[t]) == sorted(ref["ids"][i])]
+    assert len(agree) >= len(rows) - max(1, near)
+    out = dev.out.cpu().numpy()
+    err = rel_rms_err(out[rows[agree]], ref["out"][agree])
+    y_err = rel_rms_err(out[rows[agree]] - L["r_attn"][rows[agree]],
+                        ref["out"][agree] - L["r_attn"][rows[agree]])
+    print("%s T=%d out_err=%.3e y_moe_err=%.3e" % (shape.name, T, err, y_err))
+    assert err <= OUT_TOL["bf16"], err
+    assert y_err <= 10 * OUT_TOL["bf16"], y_err
+
+
+def test_q4_experts_forward_given_routing():
+    shape, T = Q4_SMALL, 300
+    L = layer_host(shape, T)
+    dev = DevLayer(shape, L)
+    ids, w, s = mi.random_router_outputs(shape, T, seed=4)
+    cfg = cfg_for(shape, T)
+    ws = smr.alloc_workspace(cfg)
+    smr.experts_forward(cfg, ws, dev.t["x"], dev.t["r_attn"], to_dev(ids), to_dev(w),
+                        dev.bank("W_gate"), dev.bank("W_up"), dev.bank("W_down"), dev.out)
+    assert smr.read_device_status(cfg, ws)[0] == 0
+    ref = orc.moe_experts_forward(L, shape, ids, w.astype(np.float64))
+    assert rel_rms_err(dev.out.cpu().numpy(), ref["out"]) <= OUT_TOL["bf16"]
