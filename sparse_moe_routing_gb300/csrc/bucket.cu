@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(BucketArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   for (int i = tid; i < kBucketWarps * E; i += kBucketThreads) hist[i] = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
 
   const int seg = (P + kBucketWarps - 1) / kBucketWarps;
@@ -152,8 +154,7 @@ cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t st) {
   static int attr[64] = {};
   cudaError_t e = ensure_smem_limit(bucket_kernel, (int)smem, attr);
   if (e != cudaSuccess) return e;
-  bucket_kernel<<<1, kBucketThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(bucket_kernel, 1, kBucketThreads, smem, st, a);
 }
 
 }  // namespace moe

@@ -15,6 +15,8 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   const int t = blockIdx.x;
   const int c = blockIdx.y * blockDim.x + threadIdx.x;  // float4 column
   if (c * 4 >= a.d) return;
+  pdl_wait();
+  pdl_trigger();
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s = 0; s < a.k; ++s) {
     const int p = a.pos[(size_t)t * a.k + s];
@@ -41,6 +43,8 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(CombineArgs a) {
   const int t = blockIdx.x;
   const int c = blockIdx.y * blockDim.x + threadIdx.x;  // 4-column group
   if (c * 4 >= a.d) return;
+  pdl_wait();
+  pdl_trigger();
   const __nv_bfloat16* Y = reinterpret_cast<const __nv_bfloat16*>(a.Y);
   const __nv_bfloat16* Ys = reinterpret_cast<const __nv_bfloat16*>(a.Ys);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -58,11 +62,9 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(CombineArgs a) {
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   const int cols = a.d / 4;
-  if (a.y_bf16)
-    combine_bf16_kernel<<<dim3(a.T, (cols + 255) / 256), 256, 0, st>>>(a);
-  else
-    combine_kernel<<<dim3(a.T, (cols + 255) / 256), 256, 0, st>>>(a);
-  return cudaGetLastError();
+  const dim3 g(a.T, (cols + 255) / 256);
+  if (a.y_bf16) return launch_pdl(combine_bf16_kernel, g, 256, 0, st, a);
+  return launch_pdl(combine_kernel, g, 256, 0, st, a);
 }
 
 }  // namespace moe

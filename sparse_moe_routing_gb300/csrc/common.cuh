@@ -92,6 +92,17 @@ __device__ __forceinline__ void store_act(__nv_bfloat16* p, size_t i, float v) {
 __device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + __expf(-v)); }
 __device__ __forceinline__ float siluf_(float v) { return v / (1.0f + __expf(-v)); }
 
+// Programmatic dependent launch: every kernel is launched so that it may be
+// scheduled while its predecessor on the stream finishes. pdl_wait() blocks
+// until the predecessor grid has completed and its writes are visible, and
+// must come before the kernel's first global memory access; pdl_trigger()
+// then lets the successor grid be scheduled. Both are no-ops for a plain
+// launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -313,6 +313,8 @@ template <typename TW>
 __global__ void __launch_bounds__(kStreamThreads, 2)
     gemv_gateup_stream(GemvArgs a, int rows_per_cta, int tok_chunk, int kseg) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_wait();
+  pdl_trigger();
   const Group v = group_of(a, blockIdx.y);
   if (!v.ok) return;
   const int r_base = blockIdx.x * rows_per_cta;
@@ -443,6 +445,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     gemv_down_stream(GemvArgs a, int rows_per_cta, int tok_chunk, int kseg) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float scale[kTokMax];
+  pdl_wait();
+  pdl_trigger();
   const Group v = group_of(a, blockIdx.y);
   if (!v.ok) return;
   const int r_base = blockIdx.x * rows_per_cta;
@@ -559,9 +563,8 @@ cudaError_t launch_gateup(const GemvArgs& a, cudaStream_t st) {
   cudaError_t e = ensure_smem_limit(gemv_gateup_stream<TW>, (int)smem, limits);
   if (e != cudaSuccess) return e;
   const int rpc = rows_for(wmax, slots, kConsumers, 64);
-  gemv_gateup_stream<TW><<<dim3((wmax + rpc - 1) / rpc, slots), kStreamThreads, smem, st>>>(
-      a, rpc, chunk, kseg);
-  return cudaGetLastError();
+  return launch_pdl(gemv_gateup_stream<TW>, dim3((wmax + rpc - 1) / rpc, slots), kStreamThreads,
+                    smem, st, a, rpc, chunk, kseg);
 }
 
 template <typename TW>
@@ -576,9 +579,8 @@ cudaError_t launch_down(const GemvArgs& a, cudaStream_t st) {
   cudaError_t e = ensure_smem_limit(gemv_down_stream<TW>, (int)smem, limits);
   if (e != cudaSuccess) return e;
   const int rpc = rows_for(a.d, slots, kConsumers * kDnRows, 256);
-  gemv_down_stream<TW><<<dim3((a.d + rpc - 1) / rpc, slots), kStreamThreads, smem, st>>>(
-      a, rpc, chunk, kseg);
-  return cudaGetLastError();
+  return launch_pdl(gemv_down_stream<TW>, dim3((a.d + rpc - 1) / rpc, slots), kStreamThreads,
+                    smem, st, a, rpc, chunk, kseg);
 }
 
 }  // namespace

@@ -140,6 +140,26 @@ inline cudaError_t ensure_smem_limit(K kernel, int bytes, int* limits) {
   return e;
 }
 
+// Launches `kernel` with programmatic stream serialization: its CTAs may be
+// scheduled (and run their set-up) while the previous kernel on the stream
+// is still finishing. Every kernel of this library calls pdl_wait() before
+// its first global memory access, so only launch latency and set-up overlap.
+template <typename... P, typename... A>
+inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, A&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+}
+
 // One launcher per kernel; each returns the launch's cudaError_t.
 cudaError_t launch_router_logits(const RouterArgs& ra, bool bf16, cudaStream_t st);
 cudaError_t launch_router_topk(const TopkArgs& ta, cudaStream_t st);

@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(128) router_logits_kernel(RouterArgs a) {
   const int rows = a.E + (a.w_shared ? 1 : 0);
   const int r = blockIdx.x * 4 + warp;
   if (r >= rows) return;
+  pdl_wait();
+  pdl_trigger();
   const int t0 = blockIdx.y * kTok;
   const int nt = min(kTok, a.T - t0);
   const TA* wrow = r < a.E ? static_cast<const TA*>(a.W_router) + (size_t)r * a.d
@@ -84,6 +86,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(TopkArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= a.T) return;
+  pdl_wait();
+  pdl_trigger();
   const float* z = a.logits + (size_t)t * (a.E + 1);
   const int E = a.E, k = a.k;
 
@@ -216,6 +220,8 @@ __global__ void __launch_bounds__(256) shared_gate_kernel(RouterArgs a, float* s
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= a.T) return;
+  pdl_wait();
+  pdl_trigger();
   const TA* w = static_cast<const TA*>(a.w_shared);
   const TA* x = static_cast<const TA*>(a.x) + (size_t)t * a.d;
   float acc = 0.f;
@@ -235,24 +241,22 @@ __global__ void __launch_bounds__(256) shared_gate_kernel(RouterArgs a, float* s
 // ---------------------------------------------------------------------------
 cudaError_t launch_shared_gate(const RouterArgs& ra, float* s_out, bool bf16, cudaStream_t st) {
   if (ra.T == 0) return cudaSuccess;
-  if (bf16) shared_gate_kernel<__nv_bfloat16><<<(ra.T + 7) / 8, 256, 0, st>>>(ra, s_out);
-  else shared_gate_kernel<float><<<(ra.T + 7) / 8, 256, 0, st>>>(ra, s_out);
-  return cudaGetLastError();
+  const dim3 g((ra.T + 7) / 8);
+  if (bf16) return launch_pdl(shared_gate_kernel<__nv_bfloat16>, g, 256, 0, st, ra, s_out);
+  return launch_pdl(shared_gate_kernel<float>, g, 256, 0, st, ra, s_out);
 }
 
 cudaError_t launch_router_logits(const RouterArgs& ra, bool bf16, cudaStream_t st) {
   if (ra.T == 0) return cudaSuccess;
   const int rows = ra.E + (ra.w_shared ? 1 : 0);
   dim3 g1((rows + 3) / 4, (ra.T + 7) / 8);
-  if (bf16) router_logits_kernel<__nv_bfloat16><<<g1, 128, 0, st>>>(ra);
-  else router_logits_kernel<float><<<g1, 128, 0, st>>>(ra);
-  return cudaGetLastError();
+  if (bf16) return launch_pdl(router_logits_kernel<__nv_bfloat16>, g1, 128, 0, st, ra);
+  return launch_pdl(router_logits_kernel<float>, g1, 128, 0, st, ra);
 }
 
 cudaError_t launch_router_topk(const TopkArgs& ta, cudaStream_t st) {
   if (ta.T == 0) return cudaSuccess;
-  router_topk_kernel<<<(ta.T + 7) / 8, 256, 0, st>>>(ta);
-  return cudaGetLastError();
+  return launch_pdl(router_topk_kernel, dim3((ta.T + 7) / 8), 256, 0, st, ta);
 }
 
 }  // namespace moe

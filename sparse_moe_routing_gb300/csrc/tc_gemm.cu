@@ -149,11 +149,23 @@ struct TileInfo {
   bool shared;
 };
 
+// Item t -> (row block, N tile). Items walk bands of kBandRows consecutive
+// row blocks N tile by N tile, so the CTAs in flight at one time share each
+// weight tile across the row blocks of a band (one DRAM read, the rest L2
+// hits) while the band's activation rows stay L2-resident. The last band may
+// be narrower; the map is a bijection onto [0, n_rb) x [0, n_tiles).
+constexpr int kBandRows = 8;
+
 template <int MODE>
-__device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, int t) {
+__device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, int t, int n_rb) {
   TileInfo ti;
-  const int rb = t / a.n_tiles;
-  ti.nt = t - rb * a.n_tiles;
+  const int span = kBandRows * a.n_tiles;
+  const int band = t / span;
+  const int rb0 = band * kBandRows;
+  const int width = min(kBandRows, n_rb - rb0);
+  const int w = t - band * span;
+  const int rb = rb0 + w % width;
+  ti.nt = w / width;
   if (MODE == kTcRouter) {
     ti.g = 0;
     ti.m = rb;
@@ -291,6 +303,8 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
 
   const int n_rb = MODE == kTcRouter ? (a.T + BM - 1) / BM : *a.n_rowblocks;
   const int total = n_rb * a.n_tiles;
@@ -309,7 +323,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
     uint32_t ph = 0;
     bool alive = true;
     for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
-      const TileInfo ti = decode_tile<MODE>(a, t);
+      const TileInfo ti = decode_tile<MODE>(a, t, n_rb);
       const CUtensorMap* mA = ti.shared ? &tmA1 : &tmA0;
       const CUtensorMap* mB0 = ti.shared ? &tmB2 : &tmB0;
       const CUtensorMap* mB1 = ti.shared ? &tmB3 : &tmB1;
@@ -405,7 +419,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
     int acc = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-      const TileInfo ti = decode_tile<MODE>(a, t);
+      const TileInfo ti = decode_tile<MODE>(a, t, n_rb);
       bool ok = lane == 0 ? mbar_wait(&tfull[acc], aph) : true;
       ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
       if (!ok) {
@@ -486,7 +500,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
     uint32_t ph = 0;
     bool alive = true;
     for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
-      const TileInfo ti = decode_tile<MODE>(a, t);
+      const TileInfo ti = decode_tile<MODE>(a, t, n_rb);
       for (int kb = 0; kb < nkb; ++kb) {
         bool ok = lane == 0 ? mbar_wait(&rawfull[stage], ph) : true;
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
@@ -530,6 +544,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ perm, int k,
                                                           int row_vecs, uint4* __restrict__ out,
                                                           int P) {
+  pdl_wait();
+  pdl_trigger();
   for (int p = blockIdx.x; p < P; p += gridDim.x) {
     const size_t src = (size_t)(perm[p] / k) * row_vecs;
     const size_t dst = (size_t)p * row_vecs;
@@ -590,9 +606,8 @@ cudaError_t launch_tc(const TcMaps& maps, const TcArgs& a, int max_items, cudaSt
   int grid = tc_sm_count();
   if (max_items < grid) grid = max_items;
   if (grid < 1) grid = 1;
-  tc_gemm_kernel<MODE, Q4><<<grid, SP::kThreadsCta, SP::kBytes, st>>>(
-      maps.A0, maps.A1, maps.B0, maps.B1, maps.B2, maps.B3, a);
-  return cudaGetLastError();
+  return launch_pdl(tc_gemm_kernel<MODE, Q4>, dim3(grid), SP::kThreadsCta, SP::kBytes, st,
+                    maps.A0, maps.A1, maps.B0, maps.B1, maps.B2, maps.B3, a);
 }
 
 // 2D uint8 view of 4-bit codes [rows][K/2 bytes], box = 32 bytes (one 64-code
@@ -638,9 +653,8 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int d,
                                cudaStream_t st) {
   if (P == 0) return cudaSuccess;
   int grid = P < tc_sm_count() * 16 ? P : tc_sm_count() * 16;
-  gather_rows_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(x), perm, k, d / 8,
-                                          static_cast<uint4*>(out), P);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3(grid), 256, 0, st, static_cast<const uint4*>(x),
+                    perm, k, d / 8, static_cast<uint4*>(out), P);
 }
 
 }  // namespace moe
