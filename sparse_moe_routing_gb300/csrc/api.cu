@@ -18,7 +18,7 @@ constexpr int kTcBm = 128;  // token rows per tensor-core tile
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct Plan {
-  size_t ctrl, logits, s_shared, counts, offsets, active, perm, pos, rowblocks;
+  size_t ctrl, logits, s_shared, counts, offsets, active, perm, pos, rowblocks, cta_hist;
   size_t H, Hs, Y, Ys, Xperm, total;
 };
 
@@ -77,6 +77,7 @@ Plan make_plan(const moe_cfg_t& c) {
   p.perm = take(P * 4);
   p.pos = take(P * 4);
   p.rowblocks = take(((P + T) / kTcBm + E + 2) * 8);
+  p.cta_hist = take((size_t)bucket_ctas((int)P) * E * 4);
   p.H = take(P * I * 4);
   p.Hs = take(T * Is * 4);
   p.Y = take(P * d * 4);
@@ -190,12 +191,15 @@ bool bank_ok(const moe_bank_t& b, int dt) {
   return true;
 }
 
-moe_status_t enqueue_route(const void* x, const void* W_router, const float* bias,
-                           const void* w_shared, const moe_cfg_t* c, int32_t* ids, float* w,
-                           float* s_shared, cudaStream_t st) {
+RouterArgs router_args(const void* x, const void* W_router, const void* w_shared,
+                       const moe_cfg_t* c, float* s_shared) {
   const Plan p = make_plan(*c);
-  RouterArgs ra{x, W_router, s_shared ? w_shared : nullptr, at<float>(c, p.logits), c->T,
-                c->d_model, c->n_experts};
+  return RouterArgs{x, W_router, s_shared ? w_shared : nullptr, at<float>(c, p.logits), c->T,
+                    c->d_model, c->n_experts};
+}
+
+TopkArgs topk_args(const RouterArgs& ra, const float* bias, const moe_cfg_t* c, int32_t* ids,
+                   float* w, float* s_shared) {
   TopkArgs ta{};
   ta.logits = ra.logits;
   ta.bias = c->router == MOE_ROUTER_SIGMOID_GROUP_TOPK ? bias : nullptr;
@@ -211,6 +215,14 @@ moe_status_t enqueue_route(const void* x, const void* W_router, const float* bia
   ta.has_shared_logit = ra.w_shared ? 1 : 0;
   ta.routed_scaling = c->routed_scaling;
   ta.renorm_clamp = c->renorm_clamp;
+  return ta;
+}
+
+moe_status_t enqueue_route(const void* x, const void* W_router, const float* bias,
+                           const void* w_shared, const moe_cfg_t* c, int32_t* ids, float* w,
+                           float* s_shared, cudaStream_t st) {
+  const RouterArgs ra = router_args(x, W_router, w_shared, c, s_shared);
+  TopkArgs ta = topk_args(ra, bias, c, ids, w, s_shared);
   const bool bf16 = c->act_dtype == MOE_BF16;
   cudaError_t e;
   if (use_tc_router(*c)) {
@@ -248,9 +260,9 @@ moe_status_t enqueue_route(const void* x, const void* W_router, const float* bia
   return cuda_status(run(MOE_KERNEL_ROUTER_TOPK, st, [&] { return launch_router_topk(ta, st); }));
 }
 
-moe_status_t enqueue_bucket(const int32_t* ids, const moe_cfg_t* c, int32_t* counts,
-                            int32_t* offsets, int32_t* active, int32_t* n_active, int32_t* perm,
-                            int32_t* pos, cudaStream_t st) {
+BucketArgs bucket_args(const int32_t* ids, const moe_cfg_t* c, int32_t* counts,
+                       int32_t* offsets, int32_t* active, int32_t* n_active, int32_t* perm,
+                       int32_t* pos) {
   BucketArgs b{};
   b.ids = ids;
   b.counts = counts;
@@ -271,7 +283,44 @@ moe_status_t enqueue_bucket(const int32_t* ids, const moe_cfg_t* c, int32_t* cou
     b.bm = kTcBm;
     b.shared_rows = c->d_ff_shared > 0 ? c->T : 0;
   }
-  return cuda_status(run(MOE_KERNEL_BUCKET, st, [&] { return launch_bucket(b, st); }));
+  return b;
+}
+
+moe_status_t enqueue_bucket(const int32_t* ids, const moe_cfg_t* c, int32_t* counts,
+                            int32_t* offsets, int32_t* active, int32_t* n_active, int32_t* perm,
+                            int32_t* pos, cudaStream_t st) {
+  const BucketArgs b = bucket_args(ids, c, counts, offsets, active, n_active, perm, pos);
+  if (bucket_ctas(b.P) == 1)
+    return cuda_status(run(MOE_KERNEL_BUCKET, st, [&] { return launch_bucket(b, st); }));
+  int* cta_hist = at<int>(c, make_plan(*c).cta_hist);
+  cudaError_t e = run(MOE_KERNEL_BUCKET, st, [&] { return launch_bucket_hist(b, cta_hist, st); });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(run(MOE_KERNEL_BUCKET, st, [&] { return launch_bucket_pack(b, cta_hist, st); }));
+}
+
+// Routing and bucketing of the layer's own batch: one fused launch for small
+// batches, else the router kernels followed by the bucketing kernel.
+moe_status_t enqueue_route_bucket(const void* x, const void* W_router, const float* bias,
+                                  const void* w_shared, const moe_cfg_t* c, int32_t* ids,
+                                  float* w, float* s_shared, cudaStream_t st) {
+  const Plan p = make_plan(*c);
+  int32_t* counts = at<int32_t>(c, p.counts);
+  int32_t* offsets = at<int32_t>(c, p.offsets);
+  int32_t* active = at<int32_t>(c, p.active);
+  int32_t* n_active = &at<Ctrl>(c, 0)->n_active;
+  int32_t* perm = at<int32_t>(c, p.perm);
+  int32_t* pos = at<int32_t>(c, p.pos);
+  if (!use_tc_router(*c) && route_small_supported(c->T, c->n_experts, c->top_k)) {
+    const RouterArgs ra = router_args(x, W_router, w_shared, c, s_shared);
+    const TopkArgs ta = topk_args(ra, bias, c, ids, w, s_shared);
+    const BucketArgs b = bucket_args(ids, c, counts, offsets, active, n_active, perm, pos);
+    const bool bf16 = c->act_dtype == MOE_BF16;
+    return cuda_status(run(MOE_KERNEL_ROUTE_SMALL, st,
+                           [&] { return launch_route_small(ra, ta, b, bf16, st); }));
+  }
+  moe_status_t s = enqueue_route(x, W_router, bias, w_shared, c, ids, w, s_shared, st);
+  if (s != MOE_OK) return s;
+  return enqueue_bucket(ids, c, counts, offsets, active, n_active, perm, pos, st);
 }
 
 // Tensor-core sequence: gather X_perm, grouped gate/up (+SwiGLU) and down
@@ -409,10 +458,16 @@ moe_status_t enqueue_experts(const void* x, const float* r_attn, const float* al
   g.has_shared = c->d_ff_shared > 0 ? 1 : 0;
   const int act = c->act_dtype == MOE_BF16 ? 1 : 0;
   const int wdt = c->expert_dtype == MOE_F32 ? 0 : (c->expert_dtype == MOE_BF16 ? 1 : 2);
-  cudaError_t e = run(MOE_KERNEL_GEMV_GATEUP, st,
-                      [&] { return launch_gemv_gateup(g, act, wdt, st); });
+  // batches of a few tokens: one warp per weight row, direct loads; larger
+  // ones: the bulk-copy streaming kernels, which stage up to 8 tokens
+  const bool small = c->T <= kGemvSmallTokens;
+  cudaError_t e = run(MOE_KERNEL_GEMV_GATEUP, st, [&] {
+    return small ? launch_gemv_small(g, act, wdt, false, st) : launch_gemv_gateup(g, act, wdt, st);
+  });
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = run(MOE_KERNEL_GEMV_DOWN, st, [&] { return launch_gemv_down(g, act, wdt, st); });
+  e = run(MOE_KERNEL_GEMV_DOWN, st, [&] {
+    return small ? launch_gemv_small(g, act, wdt, true, st) : launch_gemv_down(g, act, wdt, st);
+  });
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   CombineArgs cb{r_attn, g.Y, g.has_shared ? g.Ys : nullptr, at<int32_t>(c, p.pos), out,
                  c->T, c->d_model, c->top_k, 0};
@@ -451,7 +506,7 @@ moe_status_t moe_trace_kernel(int kernel, void* const* starts, void* const* stop
     g_trace = TraceState{};
     return MOE_OK;
   }
-  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_TC_ROUTER || n <= 0 || !starts ||
+  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_ROUTE_SMALL || n <= 0 || !starts ||
       !stops || !count)
     return MOE_ERR_INVALID_ARG;
   g_trace.kernel = kernel;
@@ -596,12 +651,8 @@ moe_status_t moe_layer_forward(const void* x, const float* r_attn, const void* W
   cudaStream_t st = (cudaStream_t)stream;
   const Plan p = make_plan(*cfg);
   float* s_sh = shared ? at<float>(cfg, p.s_shared) : nullptr;
-  s = enqueue_route(x, W_router, expert_bias, shared ? w_shared : nullptr, cfg, topk_ids, weights,
-                    s_sh, st);
-  if (s != MOE_OK) return s;
-  s = enqueue_bucket(topk_ids, cfg, at<int32_t>(cfg, p.counts), at<int32_t>(cfg, p.offsets),
-                     at<int32_t>(cfg, p.active), &at<Ctrl>(cfg, 0)->n_active,
-                     at<int32_t>(cfg, p.perm), at<int32_t>(cfg, p.pos), st);
+  s = enqueue_route_bucket(x, W_router, expert_bias, shared ? w_shared : nullptr, cfg, topk_ids,
+                           weights, s_sh, st);
   if (s != MOE_OK) return s;
   return enqueue_experts(x, r_attn, weights, s_sh, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
                          cfg, out, st);

@@ -1,160 +1,127 @@
-// Counting and packing pass over the routed (token, slot) pairs ("How
-// Treebeard routes Qwen3.6 MoE tokens", "Intel SYCL path", steps 1-3): count
-// pairs per expert, exclusive-scan the counts into offsets, list the active
-// experts, and pack every pair id t*k+slot under its expert, in ascending
-// pair order within an expert (a stable counting sort).
+// Bucketing kernels (algorithm and source in bucket_core.cuh).
 //
-// One CTA of 32 warps. Warp w owns a contiguous segment of the pairs and a
-// private histogram row, so the packing phase needs no atomics: a warp ranks
-// equal experts inside each 32-pair batch with __match_any_sync and advances
-// its own cursors.
-#include "common.cuh"
-#include "kernels.h"
+// Up to kBucketOneCta pairs: one CTA of 32 warps does the whole pass.
+// Larger batches: two kernels over kSegCtas-pair segments.
+//  1. bucket_hist: each CTA histograms its segment into cta_hist[b][E]; the
+//     last CTA to finish (self-resetting arrival counter) turns the
+//     histograms into per-CTA bases (exclusive prefix over CTAs per expert),
+//     publishes counts, offsets, the active list and the row-block list.
+//  2. bucket_pack: each CTA recounts its segment per warp and places its
+//     pairs at offsets[e] + its CTA base + its warp base, stable.
+#include "bucket_core.cuh"
 
 namespace moe {
 
-constexpr int kBucketThreads = 1024;
-constexpr int kBucketWarps = kBucketThreads / 32;
+constexpr int kBucketWarps = 32;
+constexpr int kPackWarps = 8;
+constexpr int kSegPairs = 256 * 8;  // pairs per CTA of the multi-CTA pass
 
-// Exclusive scan of n (<= 32*16) ints held in smem `v` by warp 0; writes
-// `out[0..n]` (out[n] = total). Returns nothing; caller syncs.
-__device__ void warp0_exclusive_scan(const int* v, int* out, int n) {
-  const int lane = threadIdx.x & 31;
-  const int per = (n + 31) / 32;
-  const int b = lane * per, e = min(n, b + per);
-  int local = 0;
-  for (int i = b; i < e; ++i) local += v[i];
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  int run = incl - local;
-  for (int i = b; i < e; ++i) { out[i] = run; run += v[i]; }
-  if (lane == 31) out[n] = incl;
-}
-
-__global__ void __launch_bounds__(kBucketThreads) bucket_kernel(BucketArgs a) {
+__global__ void __launch_bounds__(kBucketWarps * 32) bucket_kernel(BucketArgs a) {
   extern __shared__ int smem[];
-  const int E = a.E, P = a.P;
-  int* hist = smem;                       // [32][E]: counts, then warp bases
-  int* cnt = hist + kBucketWarps * E;     // [E]
-  int* offs = cnt + E;                    // [E+1]
-  int* flag = offs + E + 1;               // [E]
-  int* aoff = flag + E;                   // [E+1]
-  int* order = aoff + E + 1;              // [E+1]  ranked group ids
-  int* nblk = order + E + 1;              // [E+1]  row blocks per ranked group
-  int* bofs = nblk + E + 1;               // [E+2]  exclusive scan of nblk
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  for (int i = tid; i < kBucketWarps * E; i += kBucketThreads) hist[i] = 0;
   pdl_wait();
   pdl_trigger();
-  __syncthreads();
+  bucket_body<kBucketWarps>(a, smem);
+}
 
-  const int seg = (P + kBucketWarps - 1) / kBucketWarps;
-  const int s0 = min(P, warp * seg), s1 = min(P, s0 + seg);
+__global__ void __launch_bounds__(kPackWarps * 32) bucket_hist_kernel(BucketArgs a, int* cta_hist) {
+  extern __shared__ int smem[];
+  __shared__ int s_last;
+  constexpr int kThreads = kPackWarps * 32;
+  const int E = a.E, tid = threadIdx.x, b = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const int s0 = min(a.P, b * kSegPairs), s1 = min(a.P, s0 + kSegPairs);
+  int* hist = smem;  // [E]
+  for (int e = tid; e < E; e += kThreads) hist[e] = 0;
+  __syncthreads();
   bool bad = false;
-  for (int i = s0 + lane; i < s1; i += 32) {
-    int e = a.ids[i];
+  for (int i = s0 + tid; i < s1; i += kThreads) {
+    int e = __ldcg(a.ids + i);
     if (e < 0 || e >= E) { bad = true; e = E - 1; }
-    atomicAdd(&hist[warp * E + e], 1);
+    atomicAdd(&hist[e], 1);
   }
-  if (__any_sync(0xffffffffu, bad) && lane == 0) report(a.ctrl, kDevBadId, kSiteBucket);
+  if (__any_sync(0xffffffffu, bad) && (tid & 31) == 0) report(a.ctrl, kDevBadId, kSiteBucket);
   __syncthreads();
+  for (int e = tid; e < E; e += kThreads) cta_hist[(size_t)b * E + e] = hist[e];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(&a.ctrl->arrive_bucket, 1u);
+    s_last = prev == gridDim.x - 1;
+    if (s_last) a.ctrl->arrive_bucket = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
 
-  for (int e = tid; e < E; e += kBucketThreads) {
+  int* cnt = smem;                   // [E]
+  int* offs = cnt + E;               // [E+1]
+  int* flag = offs + E + 1;          // [E]
+  int* aoff = flag + E;              // [E+1]
+  int* order = aoff + E + 1;         // [E+1]
+  int* nblk = order + E + 1;         // [E+1]
+  int* bofs = nblk + E + 1;          // [E+2]
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(
+      smem + ((bucket_smem_words(0, E) - 2 * kRankKeys) & ~1));  // [kRankKeys]
+  // per-CTA bases: exclusive prefix over CTAs of each expert's counts
+  for (int e = tid; e < E; e += kThreads) {
     int run = 0;
-    for (int w = 0; w < kBucketWarps; ++w) {
-      int c = hist[w * E + e];
-      hist[w * E + e] = run;
+    for (int bb = 0; bb < (int)gridDim.x; ++bb) {
+      const int c = __ldcg(cta_hist + (size_t)bb * E + e);
+      cta_hist[(size_t)bb * E + e] = run;
       run += c;
     }
     cnt[e] = run;
-    flag[e] = run > 0 ? 1 : 0;
   }
   __syncthreads();
-  if (warp == 0) {
-    warp0_exclusive_scan(cnt, offs, E);
-    __syncwarp();
-    warp0_exclusive_scan(flag, aoff, E);
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += kBucketThreads) {
-    a.counts[e] = cnt[e];
-    a.offsets[e] = offs[e];
-    if (flag[e]) a.active[aoff[e]] = e;
-  }
-  if (tid == 0) {
-    a.offsets[E] = offs[E];
-    *a.n_active = aoff[E];
-  }
-
-  // stable packing: warp w places its segment in order after the pairs of
-  // lower warps (hist now holds each warp's base inside each expert)
-  for (int base = s0; base < s1; base += 32) {
-    const int i = base + lane;
-    const bool valid = i < s1;
-    int e = -1;
-    if (valid) {
-      e = a.ids[i];
-      if (e < 0 || e >= E) e = E - 1;
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    int p = 0;
-    if (valid) {
-      p = offs[e] + hist[warp * E + e] + rank;
-      a.perm[p] = i;
-      a.pos[i] = p;
-    }
-    __syncwarp();
-    if (valid && rank == 0) hist[warp * E + e] += __popc(peers);
-    __syncwarp();
-  }
-
-  // row-block work list for the tensor-core path: groups ordered by size
-  // (largest first, ties by lower id), then the blocks of bm rows of each
-  if (a.rowblocks) {
-    __syncthreads();
-    // rank of group g among groups with rows (shared group E included)
-    const int G = E + (a.shared_rows > 0 ? 1 : 0);
-    for (int g = tid; g < G; g += kBucketThreads) {
-      const int ng = g < E ? cnt[g] : a.shared_rows;
-      int r = 0;
-      if (ng > 0) {
-        for (int h = 0; h < G; ++h) {
-          const int nh = h < E ? cnt[h] : a.shared_rows;
-          r += (nh > ng || (nh == ng && h < g)) ? 1 : 0;
-        }
-        order[r] = g;
-        nblk[r] = (ng + a.bm - 1) / a.bm;
-      }
-    }
-    __syncthreads();
-    // groups with rows occupy ranks [0, n_nonempty)
-    const int n_nonempty = aoff[E] + (a.shared_rows > 0 ? 1 : 0);
-    if (warp == 0) warp0_exclusive_scan(nblk, bofs, n_nonempty);
-    __syncthreads();
-    for (int r = warp; r < n_nonempty; r += kBucketWarps) {
-      const int g = order[r];
-      for (int m = lane; m < nblk[r]; m += 32) a.rowblocks[bofs[r] + m] = make_int2(g, m);
-    }
-    if (tid == 0) *a.n_rowblocks = bofs[n_nonempty];
-  }
+  publish_counts<kPackWarps>(a, cnt, offs, flag, aoff);
+  if (a.rowblocks) publish_rowblocks<kPackWarps>(a, cnt, aoff, order, nblk, bofs, keys);
 }
+
+__global__ void __launch_bounds__(kPackWarps * 32) bucket_pack_kernel(BucketArgs a,
+                                                                      const int* cta_base) {
+  extern __shared__ int smem[];
+  constexpr int kThreads = kPackWarps * 32;
+  const int E = a.E, tid = threadIdx.x, b = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const int s0 = min(a.P, b * kSegPairs), s1 = min(a.P, s0 + kSegPairs);
+  int* hist = smem;  // [kPackWarps][E]
+  warp_histograms<kPackWarps>(a, s0, s1, hist);
+  for (int e = tid; e < E; e += kThreads) {
+    int run = a.offsets[e] + cta_base[(size_t)b * E + e];
+    for (int w = 0; w < kPackWarps; ++w) {
+      const int c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  pack_pairs<kPackWarps>(a, s0, s1, hist);
+}
+
+int bucket_ctas(int P) { return P <= kBucketOneCta ? 1 : (P + kSegPairs - 1) / kSegPairs; }
 
 cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t st) {
   if (a.P == 0) return cudaSuccess;
-  const int words = kBucketWarps * a.E + a.E + (a.E + 1) + a.E + (a.E + 1) +
-                    3 * (a.E + 1) + 1;
-  const size_t smem = (size_t)words * sizeof(int);
+  const size_t smem = (size_t)bucket_smem_words(kBucketWarps, a.E) * sizeof(int);
   // raise the opt-in limit when this E needs more than the default
   static int attr[64] = {};
   cudaError_t e = ensure_smem_limit(bucket_kernel, (int)smem, attr);
   if (e != cudaSuccess) return e;
-  return launch_pdl(bucket_kernel, 1, kBucketThreads, smem, st, a);
+  return launch_pdl(bucket_kernel, 1, kBucketWarps * 32, smem, st, a);
+}
+
+cudaError_t launch_bucket_hist(const BucketArgs& a, int* cta_hist, cudaStream_t st) {
+  if (a.P == 0) return cudaSuccess;
+  const size_t smem = (size_t)bucket_smem_words(0, a.E) * sizeof(int);
+  return launch_pdl(bucket_hist_kernel, bucket_ctas(a.P), kPackWarps * 32, smem, st, a, cta_hist);
+}
+
+cudaError_t launch_bucket_pack(const BucketArgs& a, const int* cta_base, cudaStream_t st) {
+  if (a.P == 0) return cudaSuccess;
+  const size_t smem = (size_t)kPackWarps * a.E * sizeof(int);
+  return launch_pdl(bucket_pack_kernel, bucket_ctas(a.P), kPackWarps * 32, smem, st, a, cta_base);
 }
 
 }  // namespace moe

@@ -33,8 +33,10 @@ struct Ctrl {
   int32_t n_active;       // active routed experts (bucket)
   int32_t n_rowblocks;    // tensor-core path: (group, m-tile) row blocks
   int32_t pad0;
-  uint32_t arrive[8];     // self-resetting arrival counters
-  int32_t pad[52];
+  uint32_t arrive[8];     // self-resetting arrival counters (one per token group)
+  uint32_t arrive_all;    // self-resetting arrival counter (fused routing)
+  uint32_t arrive_bucket; // self-resetting arrival counter (multi-CTA bucketing)
+  int32_t pad[50];
 };
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
 
@@ -108,5 +110,35 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+
+// Multi-value butterfly: reduces N partial sums (N a power of two <= 32)
+// across the warp in N-1+log2(32/N) shuffles; afterwards lane l holds the
+// total of value l / (32/N).
+template <int N>
+__device__ __forceinline__ float reduce_multi(float (&v)[N], int lane) {
+  int cnt = N;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (cnt > 1) {
+      const int half = cnt / 2;
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < half) {
+          const float send = upper ? v[i] : v[i + half];
+          const float keep = upper ? v[i + half] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      cnt = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    }
+  }
+  return v[0];
+}
+// P2<X>::v = X rounded up to a power of two.
+template <int X> struct P2 { static constexpr int v = 2 * P2<(X + 1) / 2>::v; };
+template <> struct P2<1> { static constexpr int v = 1; };
 
 }  // namespace moe

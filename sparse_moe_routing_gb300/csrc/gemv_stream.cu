@@ -136,32 +136,6 @@ __device__ __forceinline__ Group group_of(const GemvArgs& a, int slot) {
   return v;
 }
 
-template <int N>
-__device__ __forceinline__ float reduce_multi(float (&v)[N], int lane) {
-  int cnt = N;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    if (cnt > 1) {
-      const int half = cnt / 2;
-      const bool upper = (lane & o) != 0;
-#pragma unroll
-      for (int i = 0; i < N / 2; ++i) {
-        if (i < half) {
-          const float send = upper ? v[i] : v[i + half];
-          const float keep = upper ? v[i + half] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-      }
-      cnt = half;
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-    }
-  }
-  return v[0];
-}
-template <int X> struct P2 { static constexpr int v = 2 * P2<(X + 1) / 2>::v; };
-template <> struct P2<1> { static constexpr int v = 1; };
-
 // 8-element chunk c of a row (bf16 or f32) in shared memory, as floats
 template <typename TW> struct Ch;
 template <> struct Ch<__nv_bfloat16> {

@@ -164,12 +164,31 @@ inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_
 cudaError_t launch_router_logits(const RouterArgs& ra, bool bf16, cudaStream_t st);
 cudaError_t launch_router_topk(const TopkArgs& ta, cudaStream_t st);
 cudaError_t launch_shared_gate(const RouterArgs& ra, float* s_out, bool bf16, cudaStream_t st);
+// Bucketing: one CTA (launch_bucket) up to kBucketOneCta pairs, else
+// launch_bucket_hist then launch_bucket_pack over bucket_ctas(P) segments,
+// with per-CTA histograms (then bases) in cta_hist [bucket_ctas(P)][E] ints.
+constexpr int kBucketOneCta = 4096;
+int bucket_ctas(int P);
 cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t st);
+cudaError_t launch_bucket_hist(const BucketArgs& a, int* cta_hist, cudaStream_t st);
+cudaError_t launch_bucket_pack(const BucketArgs& a, const int* cta_base, cudaStream_t st);
 // act: 0 f32, 1 bf16; wdt: 0 f32, 1 bf16, 2 q4
 cudaError_t launch_gemv_gateup(const GemvArgs& a, int act, int wdt, cudaStream_t st);
 cudaError_t launch_gemv_down(const GemvArgs& a, int act, int wdt, cudaStream_t st);
+// Direct-load GEMV for batches of at most kGemvSmallTokens tokens
+// (gemv_small.cu): down = false runs gate/up + SwiGLU, true runs down x alpha.
+constexpr int kGemvSmallTokens = 4;
+cudaError_t launch_gemv_small(const GemvArgs& a, int act, int wdt, bool down, cudaStream_t st);
 // True when the GEMV kernels can stage at least one token of width d and kmax.
 bool gemv_supported(int d, int kmax);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+
+// Routing + bucketing of a batch of at most kSmallMaxTokens tokens in one
+// launch (route_small.cu); the arguments are those of the three separate
+// kernels and must describe the same batch.
+constexpr int kSmallMaxTokens = 64;
+bool route_small_supported(int T, int E, int k);
+cudaError_t launch_route_small(const RouterArgs& ra, const TopkArgs& ta, const BucketArgs& ba,
+                               bool bf16, cudaStream_t st);
 
 }  // namespace moe

@@ -1,0 +1,251 @@
+// Router device code shared by the router kernels: the logit dot products
+// z = W_router x (plus the shared-gate logit w_shared . x as column E) and
+// the routing rule per token.
+//
+// Routing rules:
+//  * softmax top-k ("How Treebeard routes Qwen3.6 MoE tokens", "Routing
+//    math"; Edge0 "Softmax top-k"): p = softmax(z); the k largest; alpha =
+//    p_sel / max(sum p_sel, clamp), times routed_scaling.
+//  * sigmoid group top-k (Edge0 "Sigmoid group top-k"): s = sigmoid(z) in
+//    fp32, selection score s + bias, contiguous groups ranked by the sum of
+//    their two largest selection scores, best topk_group groups kept, the k
+//    largest selection scores among them; alpha = s_sel / sum s_sel times
+//    routed_scaling.
+// Ties go to the lower expert (group) index; slots are written in
+// descending score order. Softmax ranking uses the fp32 logits, which orders
+// experts exactly as p does without the ties that rounding exp could create.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+#include <math.h>
+
+namespace moe {
+
+// Dot products of one router row with up to KTOK consecutive tokens (x rows
+// d elements apart), by one whole warp; afterwards every lane holds the sums
+// acc[t] for t < nt.
+template <typename TA, int KTOK>
+__device__ __forceinline__ void router_row_dots(const TA* wrow, const TA* x, int d, int nt,
+                                                int lane, float* acc) {
+  constexpr int kVec = Chunk<TA>::kVec;
+#pragma unroll
+  for (int t = 0; t < KTOK; ++t) acc[t] = 0.f;
+  const int nvec = d / kVec;
+  if (nt == 1) {
+    // one token: kU weight and kU activation chunks per lane in flight
+    constexpr int kU = 8;
+    const uint4* xr = reinterpret_cast<const uint4*>(x);
+    for (int c0 = lane; c0 < nvec; c0 += 32 * kU) {
+      uint4 wv[kU], xv[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + 32 * u;
+        wv[u] = c < nvec ? ldg_stream(wrow + (size_t)c * kVec) : make_uint4(0, 0, 0, 0);
+        xv[u] = c < nvec ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        float w[kVec], xf[kVec];
+        Chunk<TA>::unpack(wv[u], w);
+        Chunk<TA>::unpack(xv[u], xf);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) acc[0] = fmaf(w[j], xf[j], acc[0]);
+      }
+    }
+    acc[0] = warp_sum(acc[0]);
+    return;
+  }
+  // several tokens: one weight chunk and every token's chunk per step
+#pragma unroll 2
+  for (int c = lane; c < nvec; c += 32) {
+    float w[kVec];
+    Chunk<TA>::unpack(ldg_stream(wrow + (size_t)c * kVec), w);
+#pragma unroll
+    for (int t = 0; t < KTOK; ++t) {
+      if (t < nt) {
+        float xv[kVec];
+        Chunk<TA>::unpack(__ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + c), xv);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) acc[t] = fmaf(w[j], xv[j], acc[t]);
+      }
+    }
+  }
+  constexpr int NV = P2<KTOK>::v;
+  float v[NV];
+#pragma unroll
+  for (int t = 0; t < NV; ++t) v[t] = t < KTOK ? acc[t] : 0.f;
+  const float sum = reduce_multi<NV>(v, lane);
+  // lane l holds the total of token l / (32 / NV); gather them to every lane
+#pragma unroll
+  for (int t = 0; t < KTOK; ++t) acc[t] = __shfl_sync(0xffffffffu, sum, t * (32 / NV));
+}
+
+// ---------------------------------------------------------------------------
+// top-k: one warp per token; lane l owns experts l, l+32, ... (E <= 512)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void argmax_merge(float& v, int& i, float ov, int oi) {
+  if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+}
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    argmax_merge(v, i, ov, oi);
+  }
+}
+
+// NaN keys rank as -inf so that every unselected expert stays selectable.
+__device__ __forceinline__ float rank_key(float v) { return isnan(v) ? -INFINITY : v; }
+
+// Order-preserving map of a non-NaN float to an unsigned key (larger float,
+// larger key; -0 and +0 map to the same key). Every float maps above 0, so 0
+// marks an expert that can no longer be selected.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t b = __float_as_uint(f == 0.f ? 0.f : f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float order_key_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// The routing rule for token t, run by one whole warp (lane = lane index).
+// Logits are read through L2 (ld.global.cg): the fused small-batch kernel
+// hands them over between CTAs.
+__device__ __forceinline__ void topk_token(const TopkArgs& a, int t, int lane) {
+  constexpr int kMaxPerLane = 16;  // E <= 512
+  const float* z = a.logits + (size_t)t * (a.E + 1);
+  const int E = a.E, k = a.k;
+
+  float key[kMaxPerLane];   // ranking key per owned expert
+  float val[kMaxPerLane];   // softmax: logit; sigmoid: raw score s
+#pragma unroll
+  for (int j = 0; j < kMaxPerLane; ++j) {
+    int e = lane + 32 * j;
+    float zv = e < E ? __ldcg(z + e) : -INFINITY;
+    if (a.kind == 0) {
+      key[j] = e < E ? rank_key(zv) : -INFINITY;
+      val[j] = zv;
+    } else {
+      float s = 1.0f / (1.0f + expf(-zv));
+      float b = (a.bias && e < E) ? a.bias[e] : 0.0f;
+      key[j] = e < E ? rank_key(s + b) : -INFINITY;
+      val[j] = s;
+    }
+  }
+  uint32_t taken = 0;  // bit j: expert lane+32j already selected
+  // experts beyond E can never be selected
+#pragma unroll
+  for (int j = 0; j < kMaxPerLane; ++j)
+    if (lane + 32 * j >= E) taken |= 1u << j;
+
+  if (a.kind == 1) {
+    // group ranking: group g scores the sum of its two largest selection
+    // scores (all members when a group has one member)
+    const int G = E / a.n_group;
+    float gscore = -INFINITY;
+    // each group's top-2 is gathered by a warp-wide scan over its members
+    uint32_t kept = 0;
+    float my_gscore = -INFINITY;
+    for (int g = 0; g < a.n_group; ++g) {
+      float t1 = -INFINITY, t2 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kMaxPerLane; ++j) {
+        int e = lane + 32 * j;
+        if (e < E && e / G == g) {
+          float v = key[j];
+          if (v > t1) { t2 = t1; t1 = v; } else if (v > t2) { t2 = v; }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        float o1 = __shfl_xor_sync(0xffffffffu, t1, o);
+        float o2 = __shfl_xor_sync(0xffffffffu, t2, o);
+        // merge two sorted pairs (t1 >= t2), (o1 >= o2) into the top two
+        float n1 = fmaxf(t1, o1);
+        float n2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
+        t1 = n1; t2 = n2;
+      }
+      float sc = G >= 2 ? t1 + t2 : t1;
+      if (lane == g) my_gscore = sc;
+    }
+    gscore = lane < a.n_group ? my_gscore : -INFINITY;
+    for (int r = 0; r < a.topk_group; ++r) {
+      float v = lane < a.n_group ? gscore : -INFINITY;
+      int i = lane < a.n_group ? lane : 0x7fffffff;
+      if (lane < a.n_group && ((kept >> lane) & 1u)) { v = -INFINITY; i = 0x7fffffff; }
+      warp_argmax(v, i);
+      if (i < a.n_group) kept |= 1u << i;
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) {
+      int e = lane + 32 * j;
+      if (e < E && !((kept >> (e / G)) & 1u)) taken |= 1u << j;
+    }
+  }
+
+  // k rounds of warp arg-max over the untaken experts: each lane offers its
+  // largest key (lowest expert on ties), the warp takes the largest offer and
+  // the lowest expert index among equal offers (two redux instructions)
+  uint32_t okey[kMaxPerLane];
+#pragma unroll
+  for (int j = 0; j < kMaxPerLane; ++j) okey[j] = ((taken >> j) & 1u) ? 0u : order_key(key[j]);
+  int my_id = 0;
+  float my_val = 0.f;
+  for (int s = 0; s < k; ++s) {
+    uint32_t bk = 0;
+    int bj = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j)
+      if (okey[j] > bk) { bk = okey[j]; bj = j; }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t cand = bk == m ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+    // m == 0 (no candidate left) is unreachable for validated shapes
+    const int i = (int)__reduce_min_sync(0xffffffffu, cand);
+    const int owner = i & 31, jj = i >> 5;
+    float sv = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j)
+      if (j == jj) sv = val[j];
+    sv = __shfl_sync(0xffffffffu, sv, owner);
+    if (lane == owner) {
+#pragma unroll
+      for (int j = 0; j < kMaxPerLane; ++j)
+        if (j == jj) okey[j] = 0u;
+    }
+    if (lane == s) { my_id = i; my_val = sv; }
+  }
+
+  float w;
+  if (a.kind == 0) {
+    // softmax over all E logits; renormalise the selected probabilities
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j)
+      if (lane + 32 * j < E) m = fmaxf(m, val[j]);
+    m = order_key_inv(__reduce_max_sync(0xffffffffu, order_key(rank_key(m))));
+    float S = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j)
+      if (lane + 32 * j < E) S += expf(val[j] - m);
+    S = warp_sum(S);
+    float p = lane < k ? expf(my_val - m) / S : 0.f;
+    float denom = fmaxf(warp_sum(p), a.renorm_clamp);
+    w = p / denom * a.routed_scaling;
+  } else {
+    float s = lane < k ? my_val : 0.f;
+    float denom = fmaxf(warp_sum(s), 1.17549435e-38f);
+    w = s / denom * a.routed_scaling;
+  }
+  if (lane < k) {
+    a.topk_ids[(size_t)t * k + lane] = my_id;
+    a.weights[(size_t)t * k + lane] = w;
+  }
+  if (lane == 0 && a.s_shared && a.has_shared_logit)
+    a.s_shared[t] = 1.0f / (1.0f + expf(-__ldcg(z + E)));
+}
+
+
+}  // namespace moe

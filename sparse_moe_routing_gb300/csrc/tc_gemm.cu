@@ -138,6 +138,14 @@ __device__ __forceinline__ void st_shared_v4(void* p, uint32_t a, uint32_t b, ui
                "r"(d)
                : "memory");
 }
+__device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p))
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
@@ -194,65 +202,93 @@ __device__ __forceinline__ void give_up(const TcArgs& a, volatile int* abort_fla
   report(a.ctrl, kDevTimeout, site);
 }
 
+// Down epilogue staging: per epilogue warp, 32 rows x 128 B of bf16 output
+// (64 columns), rows padded to 144 B so that both the row-wise writes and the
+// column-wise reads of the transpose are free of bank conflicts.
+constexpr int kEpiRowBytes = 144;
+constexpr int kEpiWarpBytes = 32 * kEpiRowBytes;
+
+// 4-bit weights: warps 6 .. 6 + kDequantWarps - 1 dequantise the B stages,
+// one B row (of 256) per thread.
+constexpr int kDequantWarps = 8;
+
 // Shared-memory plan of one CTA (1024-byte aligned stages).
 template <bool Q4>
 struct SmemPlan {
   static constexpr int kStages = Q4 ? 3 : 4;
   static constexpr int kStageQ = 256 * (BK / 2);  // raw 4-bit codes of one B stage
-  static constexpr int kThreadsCta = Q4 ? 320 : 192;
+  static constexpr int kThreadsCta = Q4 ? 192 + 32 * kDequantWarps : 192;
   static constexpr size_t kA = 0;
   static constexpr size_t kB = kA + (size_t)kStages * kStageA;
   static constexpr size_t kQ = kB + (size_t)kStages * kStageB;
-  static constexpr size_t kBars = kQ + (Q4 ? (size_t)kStages * kStageQ : 0);
+  static constexpr size_t kEpi = kQ + (Q4 ? (size_t)kStages * kStageQ : 0);
+  static constexpr size_t kBars = kEpi + 4 * (size_t)kEpiWarpBytes;
   static constexpr size_t kBytes = 1024 + kBars + 256;
 };
 
-// Dequantises one B stage: 256 rows x 64 codes (4-bit affine, one group per
-// row per stage) from the raw ring into bf16 in the 128-byte-swizzled K-major
-// layout that TMA would have produced for a bf16 tile. Thread `tid` (of 128)
-// handles rows tid and tid + 128.
+// The (scale, min) arrays of the B row a dequant thread owns: bank row and
+// base pointers (gate/up: rows 0-127 gate, 128-255 up of N tile nt; down:
+// 256 rows of N tile nt).
+struct QRow {
+  const __nv_bfloat16* qs;
+  const __nv_bfloat16* qm;
+  size_t grow;
+};
 template <int MODE>
-__device__ __forceinline__ void dequant_stage(const TcArgs& a, const TileInfo& ti, int kb,
-                                              const uint8_t* q_stage, uint8_t* b_stage, int tid) {
+__device__ __forceinline__ QRow q_row(const TcArgs& a, const TileInfo& ti, int r) {
+  QRow q;
+  if (MODE == kTcGateUp) {
+    q.grow = (size_t)ti.g * a.brows_routed + (size_t)ti.nt * 128 + (r & 127);
+    q.qs = r < 128 ? a.qs0 : a.qs1;
+    q.qm = r < 128 ? a.qm0 : a.qm1;
+  } else {
+    q.grow = (size_t)ti.g * a.brows_routed + (size_t)ti.nt * 256 + r;
+    q.qs = a.qs0;
+    q.qm = a.qm0;
+  }
+  return q;
+}
+
+// bf16 element j (0..7) of a 16-byte vector, as raw bits.
+__device__ __forceinline__ uint32_t bf16_at(const uint4& v, int j) {
+  const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
+  return (j & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+// Dequantises one B row of a stage: 64 4-bit codes (one affine group) into
+// 64 bf16 w = scale * q + min, written in the 128-byte-swizzled K-major
+// layout that a bf16 TMA tile would have. Arithmetic in packed bf16: a code
+// nibble e becomes the bf16 128 + e by OR-ing it into 0x4300 (2^7, mantissa
+// e), 128 is subtracted exactly, and one fused multiply-add rounds
+// scale * q + min once.
+__device__ __forceinline__ void dequant_row(const uint8_t* q_row_src, uint8_t* b_stage, int r,
+                                            uint32_t scale_bits, uint32_t min_bits) {
+  const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)scale_bits),
+                                                __ushort_as_bfloat16((unsigned short)scale_bits));
+  const __nv_bfloat162 m2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)min_bits),
+                                                __ushort_as_bfloat16((unsigned short)min_bits));
+  const __nv_bfloat162 b128 = __float2bfloat162_rn(128.0f);
+  const uint4 c0 = reinterpret_cast<const uint4*>(q_row_src)[0];
+  const uint4 c1 = reinterpret_cast<const uint4*>(q_row_src)[1];
+  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  uint8_t* row_base = b_stage + (r >> 3) * 1024 + (r & 7) * 128;
+  auto deq = [&](uint32_t pair_bits) {  // (128 + e_lo, 128 + e_hi) -> (w_lo, w_hi)
+    __nv_bfloat162 q = *reinterpret_cast<__nv_bfloat162*>(&pair_bits);
+    const __nv_bfloat162 w = __hfma2(__hsub2(q, b128), s2, m2);
+    return *reinterpret_cast<const uint32_t*>(&w);
+  };
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = tid + 128 * h;
-    // global row of this B row in its bank, and its (scale, min) arrays
-    const __nv_bfloat16* qs;
-    const __nv_bfloat16* qm;
-    size_t grow;
-    if (MODE == kTcGateUp) {
-      const int rr = r & 127;
-      grow = (size_t)ti.g * a.brows_routed + (size_t)ti.nt * 128 + rr;
-      qs = r < 128 ? a.qs0 : a.qs1;
-      qm = r < 128 ? a.qm0 : a.qm1;
-    } else {
-      grow = (size_t)ti.g * a.brows_routed + (size_t)ti.nt * 256 + r;
-      qs = a.qs0;
-      qm = a.qm0;
-    }
-    const size_t gi = grow * a.qgroups + kb;
-    const float scale = __bfloat162float(qs[gi]);
-    const float mn = __bfloat162float(qm[gi]);
-    const uint4 c0 = reinterpret_cast<const uint4*>(q_stage + r * 32)[0];
-    const uint4 c1 = reinterpret_cast<const uint4*>(q_stage + r * 32)[1];
-    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    uint8_t* row_base = b_stage + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      // word c holds elements 8c..8c+7, the even element in the low nibble
-      const uint32_t w = words[c];
-      uint32_t packed[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t byte = (w >> (8 * b)) & 0xFFu;
-        // exact small-integer to float: 2^23 + q has q in its low mantissa bits
-        const float q0 = __uint_as_float(0x4B000000u | (byte & 0xFu)) - 8388608.0f;
-        const float q1 = __uint_as_float(0x4B000000u | (byte >> 4)) - 8388608.0f;
-        packed[b] = pack_bf16x2(fmaf(scale, q0, mn), fmaf(scale, q1, mn));
-      }
-      st_shared_v4(row_base + ((c ^ (r & 7)) << 4), packed[0], packed[1], packed[2], packed[3]);
-    }
+  for (int c = 0; c < 8; ++c) {
+    // word c holds elements 8c..8c+7, the even element in the low nibble:
+    // element e at bits 4e..4e+3
+    const uint32_t x = words[c];
+    const uint32_t h04 = deq((x & 0x000F000Fu) | 0x43004300u);          // e0, e4
+    const uint32_t h15 = deq(((x >> 4) & 0x000F000Fu) | 0x43004300u);   // e1, e5
+    const uint32_t h26 = deq(((x >> 8) & 0x000F000Fu) | 0x43004300u);   // e2, e6
+    const uint32_t h37 = deq(((x >> 12) & 0x000F000Fu) | 0x43004300u);  // e3, e7
+    st_shared_v4(row_base + ((c ^ (r & 7)) << 4), __byte_perm(h04, h15, 0x5410),
+                 __byte_perm(h26, h37, 0x5410), __byte_perm(h04, h15, 0x7632),
+                 __byte_perm(h26, h37, 0x7632));
   }
 }
 
@@ -270,6 +306,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
   uint8_t* sA = smem + SP::kA;
   uint8_t* sB = smem + SP::kB;
   uint8_t* sQ = smem + SP::kQ;
+  uint8_t* sEpi = smem + SP::kEpi;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SP::kBars);
   uint64_t* empty = full + STAGES;
   uint64_t* rawfull = empty + STAGES;   // Q4 only: A tile + raw codes landed
@@ -282,7 +319,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
   const int site = MODE == kTcGateUp ? kSiteTcGateUp : (MODE == kTcDown ? kSiteTcDown : kSiteTcRouter);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], Q4 ? 4 : 1);  // Q4: one arrival per dequant warp
+      mbar_init(&full[s], Q4 ? kDequantWarps : 1);  // Q4: one arrival per dequant warp
       mbar_init(&empty[s], 1);
       mbar_init(&rawfull[s], 1);
     }
@@ -453,24 +490,41 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
           }
         }
       } else if (MODE == kTcDown) {
+        // Each thread scales and packs its own row (64 columns = 128 B per
+        // step) into the warp's staging rows; the warp then stores 4 rows x
+        // 128 B per instruction, whole cache lines instead of 16 B pieces of
+        // 32 rows.
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ti.shared ? a.out_shared : a.out_routed);
-        __nv_bfloat16* dst = out + (size_t)(ti.row0 + i) * a.ld_out + ti.nt * a.bn;
         float scale = 0.f;
         if (valid) scale = ti.shared ? a.s_shared[i] : a.alpha[a.perm[ti.row0 + i]];
-        for (int c0 = 0; c0 < a.bn; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tbase + c0, v);
+        uint8_t* wbuf = sEpi + (size_t)(warp - 2) * kEpiWarpBytes;
+        uint8_t* myrow = wbuf + lane * kEpiRowBytes;
+        const int rsub = lane >> 3, ch = lane & 7;  // store phase: row in a group of 4, chunk
+        for (int c0 = 0; c0 < a.bn; c0 += 64) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tbase + c0, v0);
+          tmem_ld32(tbase + c0 + 32, v1);
           tmem_ld_wait();
-          if (valid) {
-            uint32_t h[16];
+          auto pk = [&](const uint32_t* v, int o) {
+            return pack_bf16x2(scale * __uint_as_float(v[o]), scale * __uint_as_float(v[o + 1]));
+          };
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              h[j] = pack_bf16x2(scale * __uint_as_float(v[2 * j]),
-                                 scale * __uint_as_float(v[2 * j + 1]));
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-              st_global_v4(dst + c0 + 8 * w, h[4 * w], h[4 * w + 1], h[4 * w + 2], h[4 * w + 3]);
+          for (int w = 0; w < 4; ++w) {
+            st_shared_v4(myrow + 16 * w, pk(v0, 8 * w), pk(v0, 8 * w + 2), pk(v0, 8 * w + 4),
+                         pk(v0, 8 * w + 6));
+            st_shared_v4(myrow + 64 + 16 * w, pk(v1, 8 * w), pk(v1, 8 * w + 2), pk(v1, 8 * w + 4),
+                         pk(v1, 8 * w + 6));
           }
+          __syncwarp();
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const int rr = 4 * g + rsub;                  // row within the warp's 32
+            const int gi = ti.m * BM + q * 32 + rr;       // row inside the group
+            const uint4 v = ld_shared_v4(wbuf + rr * kEpiRowBytes + ch * 16);
+            __nv_bfloat16* dst = out + (size_t)(ti.row0 + gi) * a.ld_out + ti.nt * a.bn + c0;
+            if (gi < ti.rows) st_global_v4(dst + ch * 8, v.x, v.y, v.z, v.w);
+          }
+          __syncwarp();
         }
       } else {
         float* out = static_cast<float*>(a.out_routed) + (size_t)i * a.ld_out + ti.nt * a.bn;
@@ -492,16 +546,45 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
     }
   } else if (Q4) {
     // --------------------------------------------------------------- dequant
-    // Warps 6-9 follow the producer's (tile, k-block) order: wait for the raw
-    // stage, write the bf16 B stage, make the generic-proxy writes visible to
-    // the tensor core's async proxy, then arrive on full[] (one per warp).
-    const int tid = threadIdx.x - 192;
+    // The dequant warps follow the producer's (tile, k-block) order: wait for
+    // the raw stage, write the bf16 B stage, make the generic-proxy writes
+    // visible to the tensor core's async proxy, then arrive on full[] (one
+    // arrival per warp). Thread r owns B row r. When a row's group count is a
+    // multiple of 8, its scales and mins are read 8 groups (16 B) at a time,
+    // one block of 8 k-blocks ahead of use.
+    const int r = threadIdx.x - 192;
+    const bool vec = (a.qgroups & 7) == 0;
     int stage = 0;
     uint32_t ph = 0;
     bool alive = true;
     for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
       const TileInfo ti = decode_tile<MODE>(a, t, n_rb);
+      const QRow qr = q_row<MODE>(a, ti, r);
+      const uint4* sv = reinterpret_cast<const uint4*>(qr.qs + qr.grow * a.qgroups);
+      const uint4* mv = reinterpret_cast<const uint4*>(qr.qm + qr.grow * a.qgroups);
+      uint4 sc{}, mn{}, sc_next{}, mn_next{};
+      if (vec) {
+        sc_next = __ldg(sv);
+        mn_next = __ldg(mv);
+      }
       for (int kb = 0; kb < nkb; ++kb) {
+        uint32_t sbits, mbits;
+        if (vec) {
+          if ((kb & 7) == 0) {
+            sc = sc_next;
+            mn = mn_next;
+            if (kb + 8 < nkb) {
+              sc_next = __ldg(sv + (kb >> 3) + 1);
+              mn_next = __ldg(mv + (kb >> 3) + 1);
+            }
+          }
+          sbits = bf16_at(sc, kb & 7);
+          mbits = bf16_at(mn, kb & 7);
+        } else {
+          const size_t gi = qr.grow * a.qgroups + kb;
+          sbits = __bfloat16_as_ushort(qr.qs[gi]);
+          mbits = __bfloat16_as_ushort(qr.qm[gi]);
+        }
         bool ok = lane == 0 ? mbar_wait(&rawfull[stage], ph) : true;
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
         if (!ok) {
@@ -509,7 +592,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
           alive = false;
           break;
         }
-        dequant_stage<MODE>(a, ti, kb, sQ + stage * SP::kStageQ, sB + stage * kStageB, tid);
+        dequant_row(sQ + stage * SP::kStageQ + r * 32, sB + stage * kStageB, r, sbits, mbits);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[stage]);

@@ -65,7 +65,10 @@ def _run_layer(shape, T, path=smr.PATH_AUTO):
 CASES = [
     (mi.TINY_F32, 32, 32),
     (mi.TINY_F32.with_(name="tiny_f32_ragged"), 37, 37),
+    (mi.TINY_F32.with_(name="tiny_f32_t4"), 4, 4),
     (mi.QWEN36, 1, 1),
+    (mi.QWEN36, 2, 2),
+    (mi.QWEN36, 3, 3),
     (mi.QWEN36, 8, 8),
     (mi.QWEN36, 64, 64),
     (mi.QWEN36, 37, 37),
@@ -154,11 +157,13 @@ def test_bucket_parity(T, k, E):
     assert pos.cpu().numpy().tolist() == ref["pos"].tolist()
 
 
-def test_bucket_flags_out_of_range_ids():
-    T, k, E = 16, 4, 16
+@pytest.mark.parametrize("T", [16, 3000], ids=["one-cta", "multi-cta"])
+def test_bucket_flags_out_of_range_ids(T):
+    k, E = 4, 16
     ids = np.arange(T * k, dtype=np.int32).reshape(T, k) % E
     ids[3, 1] = E + 5
     ids[7, 0] = -1
+    ids[T - 1, 3] = 1 << 30
     cfg = smr.MoEConfig(T=T, d_model=64, n_experts=E, top_k=k, d_ff=64, d_ff_shared=0)
     ws = smr.alloc_workspace(cfg)
     i32 = lambda n: torch.zeros((n,), dtype=torch.int32, device="cuda")
@@ -199,6 +204,27 @@ def test_experts_forward_parity_given_routing(shape, T, n_check):
         assert err <= OUT_TOL[shape.act_dtype], err
 
 
+@pytest.mark.parametrize("shape,T", [(mi.QWEN36, 2), (mi.TINY_F32, 3)], ids=["qwen-T2", "tiny-T3"])
+def test_small_gemv_with_an_expert_repeated_within_a_token(shape, T):
+    """Caller-given ids may name one expert in several slots of a token, so an
+    expert's group can hold more pairs than the batch has tokens; the
+    direct-load GEMV then walks the group in token chunks."""
+    L = layer_host(shape, T)
+    dev = DevLayer(shape, L)
+    ids, w, s = mi.random_router_outputs(shape, T)
+    ids[:, : shape.top_k // 2] = 3          # expert 3 in half the slots of every token
+    cfg = cfg_for(shape, T, smr.PATH_GEMV)
+    ws = smr.alloc_workspace(cfg)
+    sh = dev.shared()
+    smr.experts_forward(cfg, ws, dev.t["x"], dev.t["r_attn"], to_dev(ids), to_dev(w),
+                        dev.bank("W_gate"), dev.bank("W_up"), dev.bank("W_down"), dev.out,
+                        s_shared=to_dev(s), **sh)
+    assert smr.read_device_status(cfg, ws)[0] == 0
+    ref = orc.moe_experts_forward(L, shape, ids, w.astype(np.float64), s.astype(np.float64),
+                                  np.arange(T))
+    assert rel_rms_err(dev.out.cpu().numpy(), ref["out"]) <= OUT_TOL[shape.act_dtype]
+
+
 def test_in_place_residual_update():
     shape, T = mi.QWEN36, 8
     L = layer_host(shape, T)
@@ -225,6 +251,61 @@ def test_repeat_calls_are_deterministic():
         dev.layer_forward(cfg, ws)
         assert torch.equal(dev.out, a)
         assert torch.equal(dev.ids, ids)
+
+
+SMALL_CASES = [(mi.QWEN36, 1), (mi.QWEN36, 37), (mi.QWEN36, 64), (mi.DEEPSEEK_GROUP, 8),
+               (mi.TINY_F32, 32)]
+
+
+@pytest.mark.parametrize("shape,T", SMALL_CASES,
+                         ids=["%s-T%d" % (c[0].name, c[1]) for c in SMALL_CASES])
+def test_fused_small_batch_routing_matches_separate_kernels(shape, T):
+    """The layer call routes and buckets batches of <= 64 tokens in one fused
+    launch; moe_route + moe_experts_forward run the router, routing-rule and
+    bucketing kernels separately. Same arithmetic, so ids, weights and the
+    layer output must agree bit for bit."""
+    L = layer_host(shape, T)
+    dev = DevLayer(shape, L)
+    cfg = cfg_for(shape, T)
+    ws = smr.alloc_workspace(cfg)
+    dev.layer_forward(cfg, ws)
+    assert smr.read_device_status(cfg, ws)[0] == 0
+    ids2, w2 = torch.empty_like(dev.ids), torch.empty_like(dev.w)
+    sh = dev.shared()
+    s2 = torch.empty(T, dtype=torch.float32, device="cuda") if shape.d_ff_shared else None
+    ws2 = smr.alloc_workspace(cfg)
+    smr.route(cfg, ws2, dev.t["x"], dev.t["W_router"], ids2, w2,
+              expert_bias=dev.t.get("expert_bias"), w_shared=sh["w_shared"], s_shared=s2)
+    assert torch.equal(ids2, dev.ids)
+    assert torch.equal(w2, dev.w)
+    out2 = torch.empty_like(dev.out)
+    smr.experts_forward(cfg, ws2, dev.t["x"], dev.t["r_attn"], ids2, w2, dev.bank("W_gate"),
+                        dev.bank("W_up"), dev.bank("W_down"), out2, s_shared=s2, **sh)
+    assert smr.read_device_status(cfg, ws2)[0] == 0
+    assert torch.equal(out2, dev.out)
+
+
+def test_fused_routing_counters_survive_changing_batch_sizes():
+    """The fused routing kernel hands work between CTAs with self-resetting
+    arrival counters in the workspace: alternating batch sizes on one
+    workspace must give the same results as fresh workspaces."""
+    shape = mi.QWEN36
+    big = cfg_for(shape, 64)
+    ws = smr.alloc_workspace(big)
+    outs = {}
+    for T in (64, 5, 1, 64, 5):
+        L = layer_host(shape, T)
+        dev = DevLayer(shape, L)
+        dev.layer_forward(cfg_for(shape, T), ws)
+        if T in outs:
+            assert torch.equal(outs[T][0], dev.out) and torch.equal(outs[T][1], dev.ids)
+        else:
+            fresh = smr.alloc_workspace(cfg_for(shape, T))
+            ref = DevLayer(shape, L)
+            ref.layer_forward(cfg_for(shape, T), fresh)
+            assert torch.equal(ref.out, dev.out) and torch.equal(ref.ids, dev.ids)
+            outs[T] = (dev.out.clone(), dev.ids.clone())
+    assert smr.read_device_status(big, ws)[0] == 0
 
 
 def test_degenerate_shapes():
