@@ -149,8 +149,7 @@ typedef enum {
   MOE_KERNEL_TC_GATEUP = 8,     /* tensor-core grouped gate/up + SwiGLU */
   MOE_KERNEL_TC_DOWN = 9,       /* tensor-core grouped down x alpha */
   MOE_KERNEL_GATHER = 10,       /* packed-row gather of x (tensor-core path) */
-  MOE_KERNEL_TC_ROUTER = 11,    /* tensor-core router contraction (T >= 128, bf16) */
-  MOE_KERNEL_ROUTE_SMALL = 12   /* router + routing rule + bucketing in one launch (T <= 64) */
+  MOE_KERNEL_TC_ROUTER = 11     /* tensor-core router contraction (T >= 128, bf16) */
 } moe_kernel_t;
 
 /* Returns the ABI version (MOE_ROUTE_ABI_VERSION). */

@@ -96,9 +96,20 @@ DEEPSEEK_GROUP = MoEShape("deepseek_group", 3, d_model=2048, n_experts=128,
 MIXTRAL = MoEShape("mixtral_bf16", 4, d_model=4096, n_experts=8, top_k=2,
                    d_ff=14336, d_ff_shared=0, tokens=(2048,))
 MIXTRAL_Q4 = MIXTRAL.with_(name="mixtral_q4", expert_dtype="q4")
+# Further expert counts from the Airframe roadmap's model table (experts /
+# top-k only; the widths are this generator's choice): DeepSeek-MoE 64/6 with
+# one shared expert, Qwen MoE 60/4 with a shared expert four experts wide, and
+# DeepSeek-V2 160/6, all softmax top-k.
+DEEPSEEK_MOE_64 = MoEShape("deepseek_moe_64", 5, d_model=2048, n_experts=64, top_k=6,
+                           d_ff=1408, d_ff_shared=1408, tokens=(1, 256))
+QWEN_MOE_60 = MoEShape("qwen_moe_60", 6, d_model=2048, n_experts=60, top_k=4,
+                       d_ff=1408, d_ff_shared=5632, tokens=(1, 5))
+DEEPSEEK_V2_160 = MoEShape("deepseek_v2_160", 7, d_model=2048, n_experts=160, top_k=6,
+                           d_ff=512, d_ff_shared=512, tokens=(64, 1024))
 
 PRESETS = {s.name: s for s in (TINY_F32, QWEN36, QWEN36_PREFILL_SKEW,
-                               DEEPSEEK_GROUP, MIXTRAL, MIXTRAL_Q4)}
+                               DEEPSEEK_GROUP, MIXTRAL, MIXTRAL_Q4, DEEPSEEK_MOE_64,
+                               QWEN_MOE_60, DEEPSEEK_V2_160)}
 
 
 # ----------------------------------------------------------------------------

@@ -80,7 +80,7 @@ _SIGS = {
 # kernel families (moe_kernel_t)
 KERNELS = {"router_logits": 1, "router_topk": 2, "shared_gate": 3, "bucket": 4,
            "gemv_gateup": 5, "gemv_down": 6, "combine": 7, "tc_gateup": 8, "tc_down": 9,
-           "gather": 10, "tc_router": 11, "route_small": 12}
+           "gather": 10, "tc_router": 11}
 
 _lib = None
 

@@ -298,29 +298,16 @@ moe_status_t enqueue_bucket(const int32_t* ids, const moe_cfg_t* c, int32_t* cou
   return cuda_status(run(MOE_KERNEL_BUCKET, st, [&] { return launch_bucket_pack(b, cta_hist, st); }));
 }
 
-// Routing and bucketing of the layer's own batch: one fused launch for small
-// batches, else the router kernels followed by the bucketing kernel.
+// Routing and bucketing of the layer's own batch.
 moe_status_t enqueue_route_bucket(const void* x, const void* W_router, const float* bias,
                                   const void* w_shared, const moe_cfg_t* c, int32_t* ids,
                                   float* w, float* s_shared, cudaStream_t st) {
   const Plan p = make_plan(*c);
-  int32_t* counts = at<int32_t>(c, p.counts);
-  int32_t* offsets = at<int32_t>(c, p.offsets);
-  int32_t* active = at<int32_t>(c, p.active);
-  int32_t* n_active = &at<Ctrl>(c, 0)->n_active;
-  int32_t* perm = at<int32_t>(c, p.perm);
-  int32_t* pos = at<int32_t>(c, p.pos);
-  if (!use_tc_router(*c) && route_small_supported(c->T, c->n_experts, c->top_k)) {
-    const RouterArgs ra = router_args(x, W_router, w_shared, c, s_shared);
-    const TopkArgs ta = topk_args(ra, bias, c, ids, w, s_shared);
-    const BucketArgs b = bucket_args(ids, c, counts, offsets, active, n_active, perm, pos);
-    const bool bf16 = c->act_dtype == MOE_BF16;
-    return cuda_status(run(MOE_KERNEL_ROUTE_SMALL, st,
-                           [&] { return launch_route_small(ra, ta, b, bf16, st); }));
-  }
   moe_status_t s = enqueue_route(x, W_router, bias, w_shared, c, ids, w, s_shared, st);
   if (s != MOE_OK) return s;
-  return enqueue_bucket(ids, c, counts, offsets, active, n_active, perm, pos, st);
+  return enqueue_bucket(ids, c, at<int32_t>(c, p.counts), at<int32_t>(c, p.offsets),
+                        at<int32_t>(c, p.active), &at<Ctrl>(c, 0)->n_active,
+                        at<int32_t>(c, p.perm), at<int32_t>(c, p.pos), st);
 }
 
 // Tensor-core sequence: gather X_perm, grouped gate/up (+SwiGLU) and down
@@ -506,7 +493,7 @@ moe_status_t moe_trace_kernel(int kernel, void* const* starts, void* const* stop
     g_trace = TraceState{};
     return MOE_OK;
   }
-  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_ROUTE_SMALL || n <= 0 || !starts ||
+  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_TC_ROUTER || n <= 0 || !starts ||
       !stops || !count)
     return MOE_ERR_INVALID_ARG;
   g_trace.kernel = kernel;

@@ -8,7 +8,7 @@
 // and a private histogram row, so the packing phase needs no atomics: a warp
 // ranks equal experts inside each 32-pair batch with __match_any_sync and
 // advances its own cursors. The expert ids are read through L2 (ld.global.cg)
-// because the fused routing kernel hands them over between CTAs.
+// because the multi-CTA pass reads them in two kernels.
 #pragma once
 
 #include "common.cuh"
@@ -86,6 +86,20 @@ __device__ __forceinline__ void publish_rowblocks(const BucketArgs& a, const int
                                                   int* bofs, unsigned long long* keys) {
   constexpr int kThreads = NW * 32;
   const int E = a.E, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // every group within one row block (decode-sized batches): the order does
+  // not matter for balance, so take the active experts in id order, then the
+  // shared expert
+  bool big = a.shared_rows > a.bm;
+  for (int g = tid; g < E; g += kThreads) big |= cnt[g] > a.bm;
+  if (!__syncthreads_or(big)) {
+    for (int e = tid; e < E; e += kThreads)
+      if (cnt[e] > 0) a.rowblocks[aoff[e]] = make_int2(e, 0);
+    if (tid == 0) {
+      if (a.shared_rows > 0) a.rowblocks[aoff[E]] = make_int2(E, 0);
+      *a.n_rowblocks = aoff[E] + (a.shared_rows > 0 ? 1 : 0);
+    }
+    return;
+  }
   const int G = E + (a.shared_rows > 0 ? 1 : 0);
   int n = 2;
   while (n < G) n <<= 1;
@@ -100,7 +114,7 @@ __device__ __forceinline__ void publish_rowblocks(const BucketArgs& a, const int
   for (int size = 2; size <= n; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int i = tid; i < n / 2; i += kThreads) {
-        const int lo = 2 * stride * (i / stride) + (i % stride);
+        const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1));
         const int hi = lo + stride;
         const bool up = (lo & size) == 0;
         const unsigned long long x = keys[lo], y = keys[hi];

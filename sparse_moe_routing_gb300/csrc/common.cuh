@@ -33,10 +33,8 @@ struct Ctrl {
   int32_t n_active;       // active routed experts (bucket)
   int32_t n_rowblocks;    // tensor-core path: (group, m-tile) row blocks
   int32_t pad0;
-  uint32_t arrive[8];     // self-resetting arrival counters (one per token group)
-  uint32_t arrive_all;    // self-resetting arrival counter (fused routing)
   uint32_t arrive_bucket; // self-resetting arrival counter (multi-CTA bucketing)
-  int32_t pad[50];
+  int32_t pad[59];
 };
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
 

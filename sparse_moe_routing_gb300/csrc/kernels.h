@@ -183,12 +183,4 @@ cudaError_t launch_gemv_small(const GemvArgs& a, int act, int wdt, bool down, cu
 bool gemv_supported(int d, int kmax);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 
-// Routing + bucketing of a batch of at most kSmallMaxTokens tokens in one
-// launch (route_small.cu); the arguments are those of the three separate
-// kernels and must describe the same batch.
-constexpr int kSmallMaxTokens = 64;
-bool route_small_supported(int T, int E, int k);
-cudaError_t launch_route_small(const RouterArgs& ra, const TopkArgs& ta, const BucketArgs& ba,
-                               bool bf16, cudaStream_t st);
-
 }  // namespace moe

@@ -30,47 +30,41 @@ template <typename TA, int KTOK>
 __device__ __forceinline__ void router_row_dots(const TA* wrow, const TA* x, int d, int nt,
                                                 int lane, float* acc) {
   constexpr int kVec = Chunk<TA>::kVec;
+  constexpr int kU = 8;  // weight chunks per lane held while the tokens stream past
 #pragma unroll
   for (int t = 0; t < KTOK; ++t) acc[t] = 0.f;
   const int nvec = d / kVec;
-  if (nt == 1) {
-    // one token: kU weight and kU activation chunks per lane in flight
-    constexpr int kU = 8;
-    const uint4* xr = reinterpret_cast<const uint4*>(x);
-    for (int c0 = lane; c0 < nvec; c0 += 32 * kU) {
-      uint4 wv[kU], xv[kU];
+  for (int c0 = lane; c0 < nvec; c0 += 32 * kU) {
+    float w[kU][kVec];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int c = c0 + 32 * u;
-        wv[u] = c < nvec ? ldg_stream(wrow + (size_t)c * kVec) : make_uint4(0, 0, 0, 0);
-        xv[u] = c < nvec ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        float w[kVec], xf[kVec];
-        Chunk<TA>::unpack(wv[u], w);
-        Chunk<TA>::unpack(xv[u], xf);
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) acc[0] = fmaf(w[j], xf[j], acc[0]);
-      }
+    for (int u = 0; u < kU; ++u) {
+      const int c = c0 + 32 * u;
+      Chunk<TA>::unpack(c < nvec ? ldg_stream(wrow + (size_t)c * kVec) : make_uint4(0, 0, 0, 0),
+                        w[u]);
     }
-    acc[0] = warp_sum(acc[0]);
-    return;
-  }
-  // several tokens: one weight chunk and every token's chunk per step
-#pragma unroll 2
-  for (int c = lane; c < nvec; c += 32) {
-    float w[kVec];
-    Chunk<TA>::unpack(ldg_stream(wrow + (size_t)c * kVec), w);
 #pragma unroll
     for (int t = 0; t < KTOK; ++t) {
       if (t < nt) {
-        float xv[kVec];
-        Chunk<TA>::unpack(__ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + c), xv);
+        const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+        uint4 xv[kU];
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) acc[t] = fmaf(w[j], xv[j], acc[t]);
+        for (int u = 0; u < kU; ++u) {
+          const int c = c0 + 32 * u;
+          xv[u] = c < nvec ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          float xf[kVec];
+          Chunk<TA>::unpack(xv[u], xf);
+#pragma unroll
+          for (int j = 0; j < kVec; ++j) acc[t] = fmaf(w[u][j], xf[j], acc[t]);
+        }
       }
     }
+  }
+  if (nt == 1) {
+    acc[0] = warp_sum(acc[0]);
+    return;
   }
   constexpr int NV = P2<KTOK>::v;
   float v[NV];
@@ -111,18 +105,36 @@ __device__ __forceinline__ float order_key_inv(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// The routing rule for token t, run by one whole warp (lane = lane index).
-// Logits are read through L2 (ld.global.cg): the fused small-batch kernel
-// hands them over between CTAs.
-__device__ __forceinline__ void topk_token(const TopkArgs& a, int t, int lane) {
-  constexpr int kMaxPerLane = 16;  // E <= 512
+// Compare-exchange of two (key, slot) candidates so that the first is the
+// better one: larger key, or equal key and lower slot (= lower expert index,
+// since lane l's slot j holds expert l + 32 j).
+__device__ __forceinline__ void cas_desc(uint32_t& ka, int& ja, uint32_t& kb, int& jb) {
+  const bool swap = kb > ka || (kb == ka && jb < ja);
+  const uint32_t tk = swap ? kb : ka;
+  const int tj = swap ? jb : ja;
+  kb = swap ? ka : kb;
+  jb = swap ? ja : jb;
+  ka = tk;
+  ja = tj;
+}
+
+// The routing rule for token t, run by one whole warp (lane = lane index);
+// PL = experts per lane (E <= 32 PL, PL a power of two). Logits are read
+// through L2 (ld.global.cg).
+//
+// Selection: each lane sorts its PL candidates (bitonic network, best
+// first); each of the k rounds then takes the warp's best lane head with two
+// redux instructions (largest key, then lowest expert among equal keys) and
+// the owning lane pops its head.
+template <int PL>
+__device__ __forceinline__ void topk_token_pl(const TopkArgs& a, int t, int lane) {
   const float* z = a.logits + (size_t)t * (a.E + 1);
   const int E = a.E, k = a.k;
 
-  float key[kMaxPerLane];   // ranking key per owned expert
-  float val[kMaxPerLane];   // softmax: logit; sigmoid: raw score s
+  float key[PL];   // ranking key per owned expert
+  float val[PL];   // softmax: logit; sigmoid: raw score s
 #pragma unroll
-  for (int j = 0; j < kMaxPerLane; ++j) {
+  for (int j = 0; j < PL; ++j) {
     int e = lane + 32 * j;
     float zv = e < E ? __ldcg(z + e) : -INFINITY;
     if (a.kind == 0) {
@@ -135,24 +147,21 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, int t, int lane) {
       val[j] = s;
     }
   }
-  uint32_t taken = 0;  // bit j: expert lane+32j already selected
-  // experts beyond E can never be selected
+  uint32_t taken = 0;  // bit j: expert lane+32j cannot be selected
 #pragma unroll
-  for (int j = 0; j < kMaxPerLane; ++j)
+  for (int j = 0; j < PL; ++j)
     if (lane + 32 * j >= E) taken |= 1u << j;
 
   if (a.kind == 1) {
     // group ranking: group g scores the sum of its two largest selection
     // scores (all members when a group has one member)
     const int G = E / a.n_group;
-    float gscore = -INFINITY;
-    // each group's top-2 is gathered by a warp-wide scan over its members
     uint32_t kept = 0;
     float my_gscore = -INFINITY;
     for (int g = 0; g < a.n_group; ++g) {
       float t1 = -INFINITY, t2 = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < kMaxPerLane; ++j) {
+      for (int j = 0; j < PL; ++j) {
         int e = lane + 32 * j;
         if (e < E && e / G == g) {
           float v = key[j];
@@ -171,7 +180,7 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, int t, int lane) {
       float sc = G >= 2 ? t1 + t2 : t1;
       if (lane == g) my_gscore = sc;
     }
-    gscore = lane < a.n_group ? my_gscore : -INFINITY;
+    const float gscore = lane < a.n_group ? my_gscore : -INFINITY;
     for (int r = 0; r < a.topk_group; ++r) {
       float v = lane < a.n_group ? gscore : -INFINITY;
       int i = lane < a.n_group ? lane : 0x7fffffff;
@@ -180,40 +189,55 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, int t, int lane) {
       if (i < a.n_group) kept |= 1u << i;
     }
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j) {
+    for (int j = 0; j < PL; ++j) {
       int e = lane + 32 * j;
       if (e < E && !((kept >> (e / G)) & 1u)) taken |= 1u << j;
     }
   }
 
-  // k rounds of warp arg-max over the untaken experts: each lane offers its
-  // largest key (lowest expert on ties), the warp takes the largest offer and
-  // the lowest expert index among equal offers (two redux instructions)
-  uint32_t okey[kMaxPerLane];
+  // per-lane candidates, best first
+  uint32_t ck[PL];
+  int cj[PL];
 #pragma unroll
-  for (int j = 0; j < kMaxPerLane; ++j) okey[j] = ((taken >> j) & 1u) ? 0u : order_key(key[j]);
+  for (int j = 0; j < PL; ++j) {
+    ck[j] = ((taken >> j) & 1u) ? 0u : order_key(key[j]);
+    cj[j] = j;
+  }
+#pragma unroll
+  for (int size = 2; size <= PL; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int i = 0; i < PL; ++i) {
+        const int l = i ^ stride;
+        if (l > i) {
+          if ((i & size) == 0) cas_desc(ck[i], cj[i], ck[l], cj[l]);
+          else cas_desc(ck[l], cj[l], ck[i], cj[i]);
+        }
+      }
+    }
+  }
+
   int my_id = 0;
   float my_val = 0.f;
   for (int s = 0; s < k; ++s) {
-    uint32_t bk = 0;
-    int bj = 0;
-#pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j)
-      if (okey[j] > bk) { bk = okey[j]; bj = j; }
-    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t cand = bk == m ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+    const uint32_t m = __reduce_max_sync(0xffffffffu, ck[0]);
+    const uint32_t cand = ck[0] == m ? (uint32_t)(lane + 32 * cj[0]) : 0xffffffffu;
     // m == 0 (no candidate left) is unreachable for validated shapes
     const int i = (int)__reduce_min_sync(0xffffffffu, cand);
     const int owner = i & 31, jj = i >> 5;
     float sv = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j)
+    for (int j = 0; j < PL; ++j)
       if (j == jj) sv = val[j];
     sv = __shfl_sync(0xffffffffu, sv, owner);
-    if (lane == owner) {
+    if (lane == owner) {  // pop the head
 #pragma unroll
-      for (int j = 0; j < kMaxPerLane; ++j)
-        if (j == jj) okey[j] = 0u;
+      for (int j = 0; j + 1 < PL; ++j) {
+        ck[j] = ck[j + 1];
+        cj[j] = cj[j + 1];
+      }
+      ck[PL - 1] = 0u;
     }
     if (lane == s) { my_id = i; my_val = sv; }
   }
@@ -223,21 +247,21 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, int t, int lane) {
     // softmax over all E logits; renormalise the selected probabilities
     float m = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j)
+    for (int j = 0; j < PL; ++j)
       if (lane + 32 * j < E) m = fmaxf(m, val[j]);
     m = order_key_inv(__reduce_max_sync(0xffffffffu, order_key(rank_key(m))));
     float S = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j)
+    for (int j = 0; j < PL; ++j)
       if (lane + 32 * j < E) S += expf(val[j] - m);
     S = warp_sum(S);
     float p = lane < k ? expf(my_val - m) / S : 0.f;
     float denom = fmaxf(warp_sum(p), a.renorm_clamp);
     w = p / denom * a.routed_scaling;
   } else {
-    float s = lane < k ? my_val : 0.f;
-    float denom = fmaxf(warp_sum(s), 1.17549435e-38f);
-    w = s / denom * a.routed_scaling;
+    float sel = lane < k ? my_val : 0.f;
+    float denom = fmaxf(warp_sum(sel), 1.17549435e-38f);
+    w = sel / denom * a.routed_scaling;
   }
   if (lane < k) {
     a.topk_ids[(size_t)t * k + lane] = my_id;
@@ -247,5 +271,14 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, int t, int lane) {
     a.s_shared[t] = 1.0f / (1.0f + expf(-__ldcg(z + E)));
 }
 
+// The routing rule for token t (E <= 512), with the per-lane slot count
+// chosen from E.
+__device__ __forceinline__ void topk_token(const TopkArgs& a, int t, int lane) {
+  if (a.E <= 32) topk_token_pl<1>(a, t, lane);
+  else if (a.E <= 64) topk_token_pl<2>(a, t, lane);
+  else if (a.E <= 128) topk_token_pl<4>(a, t, lane);
+  else if (a.E <= 256) topk_token_pl<8>(a, t, lane);
+  else topk_token_pl<16>(a, t, lane);
+}
 
 }  // namespace moe

@@ -30,7 +30,7 @@ namespace moe {
 namespace {
 
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 2-5
-// epilogue, and (4-bit weights only) warps 6-9 dequantise the B stages.
+// epilogue, and (4-bit weights only) warps 6-13 dequantise the B stages.
 constexpr int BM = 128, BK = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStageA = BM * BK * 2;      // 16 KB
@@ -212,15 +212,20 @@ constexpr int kEpiWarpBytes = 32 * kEpiRowBytes;
 // one B row (of 256) per thread.
 constexpr int kDequantWarps = 8;
 
-// Shared-memory plan of one CTA (1024-byte aligned stages).
+// Shared-memory plan of one CTA (1024-byte aligned stages). bf16: kStages
+// stages of A + B. 4-bit: kStages stages of A + raw codes (filled by TMA,
+// freed by the MMA) and kBStages dequantised B stages (filled by the
+// dequant warps, freed by the MMA), so the copies run further ahead than
+// 48 KB stages would allow.
 template <bool Q4>
 struct SmemPlan {
-  static constexpr int kStages = Q4 ? 3 : 4;
+  static constexpr int kStages = Q4 ? 5 : 4;
+  static constexpr int kBStages = Q4 ? 2 : kStages;
   static constexpr int kStageQ = 256 * (BK / 2);  // raw 4-bit codes of one B stage
   static constexpr int kThreadsCta = Q4 ? 192 + 32 * kDequantWarps : 192;
   static constexpr size_t kA = 0;
   static constexpr size_t kB = kA + (size_t)kStages * kStageA;
-  static constexpr size_t kQ = kB + (size_t)kStages * kStageB;
+  static constexpr size_t kQ = kB + (size_t)kBStages * kStageB;
   static constexpr size_t kEpi = kQ + (Q4 ? (size_t)kStages * kStageQ : 0);
   static constexpr size_t kBars = kEpi + 4 * (size_t)kEpiWarpBytes;
   static constexpr size_t kBytes = 1024 + kBars + 256;
@@ -310,7 +315,9 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SP::kBars);
   uint64_t* empty = full + STAGES;
   uint64_t* rawfull = empty + STAGES;   // Q4 only: A tile + raw codes landed
-  uint64_t* tfull = rawfull + STAGES;
+  uint64_t* bfull = rawfull + STAGES;   // Q4 only: B stage dequantised
+  uint64_t* bempty = bfull + SP::kBStages;  // Q4 only: B stage consumed
+  uint64_t* tfull = bempty + SP::kBStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -319,9 +326,13 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
   const int site = MODE == kTcGateUp ? kSiteTcGateUp : (MODE == kTcDown ? kSiteTcDown : kSiteTcRouter);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], Q4 ? kDequantWarps : 1);  // Q4: one arrival per dequant warp
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&rawfull[s], 1);
+    }
+    for (int s = 0; s < SP::kBStages; ++s) {
+      mbar_init(&bfull[s], kDequantWarps);  // one arrival per dequant warp
+      mbar_init(&bempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -353,7 +364,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
   if (warp == 0) {
     // -------------------------------------------------------------- producer
     // bf16 B: A + B tiles land on full[]. Q4 B: A + raw code tiles land on
-    // rawfull[] and the dequant warps then fill the B stage.
+    // rawfull[] and the dequant warps then fill a stage of the B ring.
     const uint32_t stage_bytes =
         Q4 ? kStageA + a.bn * (BK / 2) : kStageA + a.bn * BK * 2;
     int stage = 0;
@@ -402,8 +413,8 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16(BM, a.bn);
-    int stage = 0, acc = 0;
-    uint32_t ph = 0, aph = 0;
+    int stage = 0, acc = 0, bs = 0;
+    uint32_t ph = 0, aph = 0, bph = 0;
     bool alive = true;
     for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
       bool ok = lane == 0 ? mbar_wait(&tempty[acc], aph ^ 1u) : true;
@@ -417,8 +428,12 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
       for (int kb = 0; kb < nkb; ++kb) {
         ok = true;
         if (lane == 0) {
-          ok = mbar_wait(&full[stage], ph);
-          if (Q4 && ok) ok = mbar_wait(&rawfull[stage], ph);  // the A tile of this stage
+          if (Q4) {
+            ok = mbar_wait(&rawfull[stage], ph);     // the A tile of this stage
+            if (ok) ok = mbar_wait(&bfull[bs], bph);  // its dequantised B stage
+          } else {
+            ok = mbar_wait(&full[stage], ph);
+          }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
         if (!ok) {
@@ -429,18 +444,23 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a_base = smem_u32(sA + stage * kStageA);
-          const uint32_t b_base = smem_u32(sB + stage * kStageB);
+          const uint32_t b_base = smem_u32(sB + (Q4 ? bs : stage) * kStageB);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             mma_bf16(d_tmem, sw128_desc(a_base + k * 32), sw128_desc(b_base + k * 32), idesc,
                      (kb | k) != 0 ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
+          if (Q4) mma_commit(&bempty[bs]);
         }
         __syncwarp();
         if (++stage == STAGES) {
           stage = 0;
           ph ^= 1u;
+        }
+        if (Q4 && ++bs == SP::kBStages) {
+          bs = 0;
+          bph ^= 1u;
         }
       }
       if (!alive) break;
@@ -554,8 +574,8 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
     // one block of 8 k-blocks ahead of use.
     const int r = threadIdx.x - 192;
     const bool vec = (a.qgroups & 7) == 0;
-    int stage = 0;
-    uint32_t ph = 0;
+    int stage = 0, bs = 0;
+    uint32_t ph = 0, bph = 0;
     bool alive = true;
     for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
       const TileInfo ti = decode_tile<MODE>(a, t, n_rb);
@@ -585,20 +605,28 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
           sbits = __bfloat16_as_ushort(qr.qs[gi]);
           mbits = __bfloat16_as_ushort(qr.qm[gi]);
         }
-        bool ok = lane == 0 ? mbar_wait(&rawfull[stage], ph) : true;
+        bool ok = true;
+        if (lane == 0) {
+          ok = mbar_wait(&rawfull[stage], ph);
+          if (ok) ok = mbar_wait(&bempty[bs], bph ^ 1u);
+        }
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
         if (!ok) {
           if (lane == 0) give_up(a, abort_flag, site);
           alive = false;
           break;
         }
-        dequant_row(sQ + stage * SP::kStageQ + r * 32, sB + stage * kStageB, r, sbits, mbits);
+        dequant_row(sQ + stage * SP::kStageQ + r * 32, sB + bs * kStageB, r, sbits, mbits);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full[stage]);
+        if (lane == 0) mbar_arrive(&bfull[bs]);
         if (++stage == STAGES) {
           stage = 0;
           ph ^= 1u;
+        }
+        if (++bs == SP::kBStages) {
+          bs = 0;
+          bph ^= 1u;
         }
       }
     }

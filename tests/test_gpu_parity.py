@@ -77,6 +77,12 @@ CASES = [
     (mi.QWEN36_PREFILL_SKEW, 4096, 24),
     (mi.DEEPSEEK_GROUP, 4096, 24),
     (mi.MIXTRAL, 2048, 6),
+    (mi.DEEPSEEK_MOE_64, 1, 1),
+    (mi.DEEPSEEK_MOE_64, 256, 12),
+    (mi.QWEN_MOE_60, 1, 1),
+    (mi.QWEN_MOE_60, 5, 5),
+    (mi.DEEPSEEK_V2_160, 64, 12),
+    (mi.DEEPSEEK_V2_160, 1024, 12),
 ]
 
 
@@ -253,17 +259,16 @@ def test_repeat_calls_are_deterministic():
         assert torch.equal(dev.ids, ids)
 
 
-SMALL_CASES = [(mi.QWEN36, 1), (mi.QWEN36, 37), (mi.QWEN36, 64), (mi.DEEPSEEK_GROUP, 8),
-               (mi.TINY_F32, 32)]
+CONSISTENCY_CASES = [(mi.QWEN36, 1), (mi.QWEN36, 37), (mi.QWEN36, 64), (mi.DEEPSEEK_GROUP, 8),
+                     (mi.TINY_F32, 32), (mi.QWEN36, 600)]
 
 
-@pytest.mark.parametrize("shape,T", SMALL_CASES,
-                         ids=["%s-T%d" % (c[0].name, c[1]) for c in SMALL_CASES])
-def test_fused_small_batch_routing_matches_separate_kernels(shape, T):
-    """The layer call routes and buckets batches of <= 64 tokens in one fused
-    launch; moe_route + moe_experts_forward run the router, routing-rule and
-    bucketing kernels separately. Same arithmetic, so ids, weights and the
-    layer output must agree bit for bit."""
+@pytest.mark.parametrize("shape,T", CONSISTENCY_CASES,
+                         ids=["%s-T%d" % (c[0].name, c[1]) for c in CONSISTENCY_CASES])
+def test_layer_matches_route_then_experts(shape, T):
+    """moe_layer_forward against moe_route followed by moe_experts_forward on
+    the same inputs: the same kernels in the same order, so ids, weights and
+    the layer output must agree bit for bit."""
     L = layer_host(shape, T)
     dev = DevLayer(shape, L)
     cfg = cfg_for(shape, T)
@@ -285,15 +290,16 @@ def test_fused_small_batch_routing_matches_separate_kernels(shape, T):
     assert torch.equal(out2, dev.out)
 
 
-def test_fused_routing_counters_survive_changing_batch_sizes():
-    """The fused routing kernel hands work between CTAs with self-resetting
-    arrival counters in the workspace: alternating batch sizes on one
-    workspace must give the same results as fresh workspaces."""
+def test_workspace_reuse_across_batch_sizes():
+    """The multi-CTA bucketing pass hands work between CTAs with a
+    self-resetting arrival counter in the workspace: alternating batch sizes
+    (one-CTA and multi-CTA bucketing) on one workspace must give the same
+    results as fresh workspaces."""
     shape = mi.QWEN36
-    big = cfg_for(shape, 64)
+    big = cfg_for(shape, 600)
     ws = smr.alloc_workspace(big)
     outs = {}
-    for T in (64, 5, 1, 64, 5):
+    for T in (600, 5, 1, 600, 64, 5):
         L = layer_host(shape, T)
         dev = DevLayer(shape, L)
         dev.layer_forward(cfg_for(shape, T), ws)
