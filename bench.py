@@ -508,6 +508,27 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def run_eager(args):
+    """N plain layer calls in a row (for ncu captures of single launches: with
+    K kernels per call, skip K*c launches to capture the (c+1)-th call)."""
+    import torch
+    import moe_inputs as mi
+    import sparse_moe_routing_gb300 as smr
+    device = torch.device("cuda", 0)
+    preset, T_default, desc = WORKLOADS[args.workload]
+    shape = mi.PRESETS[preset]
+    path = {"auto": smr.PATH_AUTO, "gemv": smr.PATH_GEMV, "tc": smr.PATH_TC}[args.path]
+    T = args.tokens or T_default
+    wl = Workload(Weights(shape, device), T, 1, path)
+    for _ in range(args.eager):
+        wl.step(0)
+    torch.cuda.synchronize()
+    st, word = smr.read_device_status(wl.cfg, wl.ws)
+    print(json.dumps({"eager_calls": args.eager, "workload": desc % T, "status": st}))
+    if st != 0:
+        sys.exit(1)
+
+
 def run_reference(args):
     """The reference arm: the fp64 oracle, as it stands, on this host's
     cores, on the same workload; each step is a bounded sample of tokens."""
@@ -565,10 +586,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--breakdown", action="store_true",
                     help="also report the mean in-graph time of every kernel family")
+    ap.add_argument("--eager", type=int, default=0, metavar="N",
+                    help="profiling aid: run N untimed eager layer calls on the workload "
+                         "(one weight copy, no graph) and exit; prints no bench line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.eager:
+        run_eager(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

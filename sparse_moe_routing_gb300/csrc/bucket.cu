@@ -63,13 +63,21 @@ __global__ void __launch_bounds__(kPackWarps * 32) bucket_hist_kernel(BucketArgs
   int* bofs = nblk + E + 1;          // [E+2]
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(
       smem + ((bucket_smem_words(0, E) - 2 * kRankKeys) & ~1));  // [kRankKeys]
-  // per-CTA bases: exclusive prefix over CTAs of each expert's counts
+  // per-CTA bases: exclusive prefix over CTAs of each expert's counts, eight
+  // CTAs' counts loaded at a time so their L2 round trips overlap
+  const int nb = (int)gridDim.x;
   for (int e = tid; e < E; e += kThreads) {
     int run = 0;
-    for (int bb = 0; bb < (int)gridDim.x; ++bb) {
-      const int c = __ldcg(cta_hist + (size_t)bb * E + e);
-      cta_hist[(size_t)bb * E + e] = run;
-      run += c;
+    for (int b0 = 0; b0 < nb; b0 += 8) {
+      int c[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        c[u] = b0 + u < nb ? __ldcg(cta_hist + (size_t)(b0 + u) * E + e) : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (b0 + u < nb) cta_hist[(size_t)(b0 + u) * E + e] = run;
+        run += c[u];
+      }
     }
     cnt[e] = run;
   }
