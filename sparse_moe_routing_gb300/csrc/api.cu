@@ -58,6 +58,17 @@ bool use_tc(const moe_cfg_t& c) {
   return c.path == MOE_PATH_AUTO && c.T >= kTcMinTokens;
 }
 
+// Paired GEMM items (two 128-row blocks per B tile) for 4-bit banks whose
+// routed experts average at least two row blocks each: pairing halves the
+// dequantisation per flop, which bounds those kernels (Mixtral-shape 4-bit
+// gate/up 1440 -> 1335 us). For bf16 banks the single-buffered accumulator
+// of paired items costs more than the B traffic it saves (Mixtral-shape bf16
+// layer 1211 -> 1431 us), so they stay unpaired.
+bool use_pair(const moe_cfg_t& c) {
+  return use_tc(c) && c.expert_dtype == MOE_Q4_AFFINE_G64 &&
+         (long long)c.T * c.top_k >= 2LL * kTcBm * c.n_experts;
+}
+
 Plan make_plan(const moe_cfg_t& c) {
   Plan p{};
   size_t off = 0;
@@ -282,6 +293,7 @@ BucketArgs bucket_args(const int32_t* ids, const moe_cfg_t* c, int32_t* counts,
     b.n_rowblocks = &at<Ctrl>(c, 0)->n_rowblocks;
     b.bm = kTcBm;
     b.shared_rows = c->d_ff_shared > 0 ? c->T : 0;
+    b.pair = use_pair(*c) ? 1 : 0;
   }
   return b;
 }
@@ -344,6 +356,7 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
   a.ctrl = ctrl;
   a.E = E;
   a.T = T;
+  a.pair = use_pair(*c) ? 1 : 0;
 
   const bool q4 = c->expert_dtype == MOE_Q4_AFFINE_G64;
   auto bmap = [&](CUtensorMap* mp, const void* w, uint64_t rows, uint64_t K, uint32_t box) {

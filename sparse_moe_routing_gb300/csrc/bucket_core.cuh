@@ -76,7 +76,8 @@ __device__ __forceinline__ void publish_counts(const BucketArgs& a, const int* c
 
 // Row-block work list for the tensor-core path: groups ordered by size
 // (largest first, ties by lower id; the shared expert is group E with
-// shared_rows rows), then the blocks of bm rows of each. The order comes
+// shared_rows rows), then the blocks of bm rows of each (every second block
+// when a.pair: each entry then stands for blocks m and m + 1). The order comes
 // from a bitonic sort of (rows descending, id ascending) keys in `keys`
 // (kRankKeys 8-byte entries); order, nblk: [E+1], bofs: [E+2] scratch. All
 // threads of the CTA call it.
@@ -132,14 +133,16 @@ __device__ __forceinline__ void publish_rowblocks(const BucketArgs& a, const int
     const unsigned long long k = keys[r];
     const int ng = (int)(0xFFFFFFFFu - (uint32_t)(k >> 32));
     order[r] = (int)(k & 0xFFFFFFFFu);
-    nblk[r] = (ng + a.bm - 1) / a.bm;
+    const int blocks = (ng + a.bm - 1) / a.bm;
+    nblk[r] = a.pair ? (blocks + 1) / 2 : blocks;  // list entries: pairs when paired
   }
   __syncthreads();
   if (warp == 0) warp0_exclusive_scan(nblk, bofs, n_nonempty);
   __syncthreads();
+  const int step = a.pair ? 2 : 1;
   for (int r = warp; r < n_nonempty; r += NW) {
     const int g = order[r];
-    for (int m = lane; m < nblk[r]; m += 32) a.rowblocks[bofs[r] + m] = make_int2(g, m);
+    for (int m = lane; m < nblk[r]; m += 32) a.rowblocks[bofs[r] + m] = make_int2(g, m * step);
   }
   if (tid == 0) *a.n_rowblocks = bofs[n_nonempty];
 }

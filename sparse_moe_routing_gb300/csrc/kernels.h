@@ -43,6 +43,7 @@ struct BucketArgs {
   int2* rowblocks;
   int32_t* n_rowblocks;
   int bm, shared_rows;    // shared_rows = T when a shared expert exists, else 0
+  int pair;               // 1: list pairs of row blocks (m even), for paired GEMM items
 };
 
 // Grouped GEMV over the packed rows ("groups" = active routed experts, then
@@ -105,6 +106,10 @@ struct TcArgs {
   const __nv_bfloat16* qs1;
   const __nv_bfloat16* qm1;
   int qgroups;                 // K / 64
+  // 1: each row-block entry is a pair of 128-row blocks (m, m + 1) sharing
+  // the B tiles (the bucketing pass then lists every second block); 4-bit
+  // banks only
+  int pair;
 };
 
 // The six operand maps: A routed/shared, B0/B1 routed, B2/B3 shared.

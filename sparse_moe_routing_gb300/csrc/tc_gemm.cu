@@ -217,14 +217,21 @@ constexpr int kDequantWarps = 8;
 // freed by the MMA) and kBStages dequantised B stages (filled by the
 // dequant warps, freed by the MMA), so the copies run further ahead than
 // 48 KB stages would allow.
-template <bool Q4>
+//
+// RB = row blocks per work item. RB = 2 ("paired" items, used for 4-bit
+// banks): two 128-row blocks of one group share each B stage (two A tiles
+// per stage, two MMAs per k-block into two 256-column accumulators that fill
+// TMEM), halving the B traffic and the dequantisation per flop; the
+// accumulator is then single-buffered.
+template <bool Q4, int RB>
 struct SmemPlan {
-  static constexpr int kStages = Q4 ? 5 : 4;
+  static constexpr int kStages = RB == 2 ? 3 : (Q4 ? 5 : 4);
   static constexpr int kBStages = Q4 ? 2 : kStages;
+  static constexpr int kNAcc = 2 / RB;   // accumulator buffers of RB x 256 TMEM columns
   static constexpr int kStageQ = 256 * (BK / 2);  // raw 4-bit codes of one B stage
   static constexpr int kThreadsCta = Q4 ? 192 + 32 * kDequantWarps : 192;
   static constexpr size_t kA = 0;
-  static constexpr size_t kB = kA + (size_t)kStages * kStageA;
+  static constexpr size_t kB = kA + (size_t)kStages * RB * kStageA;
   static constexpr size_t kQ = kB + (size_t)kBStages * kStageB;
   static constexpr size_t kEpi = kQ + (Q4 ? (size_t)kStages * kStageQ : 0);
   static constexpr size_t kBars = kEpi + 4 * (size_t)kEpiWarpBytes;
@@ -297,14 +304,15 @@ __device__ __forceinline__ void dequant_row(const uint8_t* q_row_src, uint8_t* b
   }
 }
 
-template <int MODE, bool Q4>
-__global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
+template <int MODE, bool Q4, int RB>
+__global__ void __launch_bounds__(SmemPlan<Q4, RB>::kThreadsCta, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmB3,
                    const TcArgs a) {
-  using SP = SmemPlan<Q4>;
+  using SP = SmemPlan<Q4, RB>;
   constexpr int STAGES = SP::kStages;
+  constexpr int NACC = SP::kNAcc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -334,7 +342,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
       mbar_init(&bfull[s], kDequantWarps);  // one arrival per dequant warp
       mbar_init(&bempty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NACC; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4);
     }
@@ -379,6 +387,8 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
       const int bhalf = MODE == kTcGateUp ? a.bn / 2 : a.bn;
       const int brow = (ti.shared || MODE == kTcRouter ? 0 : ti.g * a.brows_routed) +
                        ti.nt * bhalf;
+      const bool two = RB == 2 && (ti.m + 1) * BM < ti.rows;  // second row block present
+      const uint32_t item_bytes = stage_bytes + (two ? kStageA : 0);
       for (int kb = 0; kb < nkb; ++kb) {
         bool ok = lane == 0 ? mbar_wait(&empty[stage], ph ^ 1u) : true;
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
@@ -389,8 +399,9 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
         }
         if (lane == 0) {
           uint64_t* bar = Q4 ? &rawfull[stage] : &full[stage];
-          mbar_expect_tx(bar, stage_bytes);
-          tma_load_2d(sA + stage * kStageA, mA, bar, kb * BK, arow);
+          mbar_expect_tx(bar, item_bytes);
+          tma_load_2d(sA + stage * RB * kStageA, mA, bar, kb * BK, arow);
+          if (two) tma_load_2d(sA + (stage * RB + 1) * kStageA, mA, bar, kb * BK, arow + BM);
           if (Q4) {
             uint8_t* q_dst = sQ + stage * SP::kStageQ;
             tma_load_2d(q_dst, mB0, bar, kb * (BK / 2), brow);
@@ -417,6 +428,11 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
     uint32_t ph = 0, aph = 0, bph = 0;
     bool alive = true;
     for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
+      bool two = false;
+      if (RB == 2) {
+        const TileInfo ti = decode_tile<MODE>(a, t, n_rb);
+        two = (ti.m + 1) * BM < ti.rows;
+      }
       bool ok = lane == 0 ? mbar_wait(&tempty[acc], aph ^ 1u) : true;
       ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
       if (!ok) {
@@ -424,7 +440,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256 * RB);
       for (int kb = 0; kb < nkb; ++kb) {
         ok = true;
         if (lane == 0) {
@@ -443,12 +459,17 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t a_base = smem_u32(sA + stage * kStageA);
           const uint32_t b_base = smem_u32(sB + (Q4 ? bs : stage) * kStageB);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            mma_bf16(d_tmem, sw128_desc(a_base + k * 32), sw128_desc(b_base + k * 32), idesc,
-                     (kb | k) != 0 ? 1u : 0u);
+          for (int j = 0; j < RB; ++j) {
+            if (j == 0 || two) {
+              const uint32_t a_base = smem_u32(sA + (stage * RB + j) * kStageA);
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                mma_bf16(d_tmem + j * 256, sw128_desc(a_base + k * 32),
+                         sw128_desc(b_base + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
+              }
+            }
           }
           mma_commit(&empty[stage]);
           if (Q4) mma_commit(&bempty[bs]);
@@ -466,8 +487,10 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
       if (!alive) break;
       if (lane == 0) mma_commit(&tfull[acc]);
       __syncwarp();
-      acc ^= 1;
-      if (acc == 0) aph ^= 1u;
+      if (++acc == NACC) {
+        acc = 0;
+        aph ^= 1u;
+      }
     }
   } else if (warp < 6) {
     // -------------------------------------------------------------- epilogue
@@ -484,85 +507,92 @@ __global__ void __launch_bounds__(SmemPlan<Q4>::kThreadsCta, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t tbase = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(q * 32) << 16);
-      const int i = ti.m * BM + r;  // row inside the group
-      const bool valid = i < ti.rows;
-      if (MODE == kTcGateUp) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ti.shared ? a.out_shared : a.out_routed);
-        __nv_bfloat16* dst = out + (size_t)(ti.row0 + i) * a.ld_out + ti.nt * (a.bn / 2);
-        const int half = a.bn / 2;
-        for (int c0 = 0; c0 < half; c0 += 32) {
-          uint32_t g[32], u[32];
-          tmem_ld32(tbase + c0, g);
-          tmem_ld32(tbase + half + c0, u);
-          tmem_ld_wait();
-          if (valid) {
-            uint32_t h[16];
+      for (int j = 0; j < RB; ++j) {
+        const int mb = ti.m + j;  // row block of this accumulator
+        if (j > 0 && mb * BM >= ti.rows) break;
+        const uint32_t tbase =
+            tmem_base + (uint32_t)(acc * 256 * RB + j * 256) + ((uint32_t)(q * 32) << 16);
+        const int i = mb * BM + r;  // row inside the group
+        const bool valid = i < ti.rows;
+        if (MODE == kTcGateUp) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ti.shared ? a.out_shared : a.out_routed);
+          __nv_bfloat16* dst = out + (size_t)(ti.row0 + i) * a.ld_out + ti.nt * (a.bn / 2);
+          const int half = a.bn / 2;
+          for (int c0 = 0; c0 < half; c0 += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld32(tbase + c0, g);
+            tmem_ld32(tbase + half + c0, u);
+            tmem_ld_wait();
+            if (valid) {
+              uint32_t h[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
-              const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
-              h[j] = pack_bf16x2(siluf_(g0) * u0, siluf_(g1) * u1);
+              for (int j = 0; j < 16; ++j) {
+                const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+                const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+                h[j] = pack_bf16x2(siluf_(g0) * u0, siluf_(g1) * u1);
+              }
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                st_global_v4(dst + c0 + 8 * v, h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
             }
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              st_global_v4(dst + c0 + 8 * v, h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
           }
-        }
-      } else if (MODE == kTcDown) {
-        // Each thread scales and packs its own row (64 columns = 128 B per
-        // step) into the warp's staging rows; the warp then stores 4 rows x
-        // 128 B per instruction, whole cache lines instead of 16 B pieces of
-        // 32 rows.
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ti.shared ? a.out_shared : a.out_routed);
-        float scale = 0.f;
-        if (valid) scale = ti.shared ? a.s_shared[i] : a.alpha[a.perm[ti.row0 + i]];
-        uint8_t* wbuf = sEpi + (size_t)(warp - 2) * kEpiWarpBytes;
-        uint8_t* myrow = wbuf + lane * kEpiRowBytes;
-        const int rsub = lane >> 3, ch = lane & 7;  // store phase: row in a group of 4, chunk
-        for (int c0 = 0; c0 < a.bn; c0 += 64) {
-          uint32_t v0[32], v1[32];
-          tmem_ld32(tbase + c0, v0);
-          tmem_ld32(tbase + c0 + 32, v1);
-          tmem_ld_wait();
-          auto pk = [&](const uint32_t* v, int o) {
-            return pack_bf16x2(scale * __uint_as_float(v[o]), scale * __uint_as_float(v[o + 1]));
-          };
+        } else if (MODE == kTcDown) {
+          // Each thread scales and packs its own row (64 columns = 128 B per
+          // step) into the warp's staging rows; the warp then stores 4 rows x
+          // 128 B per instruction, whole cache lines instead of 16 B pieces of
+          // 32 rows.
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ti.shared ? a.out_shared : a.out_routed);
+          float scale = 0.f;
+          if (valid) scale = ti.shared ? a.s_shared[i] : a.alpha[a.perm[ti.row0 + i]];
+          uint8_t* wbuf = sEpi + (size_t)(warp - 2) * kEpiWarpBytes;
+          uint8_t* myrow = wbuf + lane * kEpiRowBytes;
+          const int rsub = lane >> 3, ch = lane & 7;  // store phase: row in a group of 4, chunk
+          for (int c0 = 0; c0 < a.bn; c0 += 64) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tbase + c0, v0);
+            tmem_ld32(tbase + c0 + 32, v1);
+            tmem_ld_wait();
+            auto pk = [&](const uint32_t* v, int o) {
+              return pack_bf16x2(scale * __uint_as_float(v[o]), scale * __uint_as_float(v[o + 1]));
+            };
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            st_shared_v4(myrow + 16 * w, pk(v0, 8 * w), pk(v0, 8 * w + 2), pk(v0, 8 * w + 4),
-                         pk(v0, 8 * w + 6));
-            st_shared_v4(myrow + 64 + 16 * w, pk(v1, 8 * w), pk(v1, 8 * w + 2), pk(v1, 8 * w + 4),
-                         pk(v1, 8 * w + 6));
+            for (int w = 0; w < 4; ++w) {
+              st_shared_v4(myrow + 16 * w, pk(v0, 8 * w), pk(v0, 8 * w + 2), pk(v0, 8 * w + 4),
+                           pk(v0, 8 * w + 6));
+              st_shared_v4(myrow + 64 + 16 * w, pk(v1, 8 * w), pk(v1, 8 * w + 2), pk(v1, 8 * w + 4),
+                           pk(v1, 8 * w + 6));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const int rr = 4 * g + rsub;                  // row within the warp's 32
+              const int gi = mb * BM + q * 32 + rr;       // row inside the group
+              const uint4 v = ld_shared_v4(wbuf + rr * kEpiRowBytes + ch * 16);
+              __nv_bfloat16* dst = out + (size_t)(ti.row0 + gi) * a.ld_out + ti.nt * a.bn + c0;
+              if (gi < ti.rows) st_global_v4(dst + ch * 8, v.x, v.y, v.z, v.w);
+            }
+            __syncwarp();
           }
-          __syncwarp();
+        } else {
+          float* out = static_cast<float*>(a.out_routed) + (size_t)i * a.ld_out + ti.nt * a.bn;
+          for (int c0 = 0; c0 < a.bn; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c0, v);
+            tmem_ld_wait();
+            if (valid) {
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const int rr = 4 * g + rsub;                  // row within the warp's 32
-            const int gi = ti.m * BM + q * 32 + rr;       // row inside the group
-            const uint4 v = ld_shared_v4(wbuf + rr * kEpiRowBytes + ch * 16);
-            __nv_bfloat16* dst = out + (size_t)(ti.row0 + gi) * a.ld_out + ti.nt * a.bn + c0;
-            if (gi < ti.rows) st_global_v4(dst + ch * 8, v.x, v.y, v.z, v.w);
-          }
-          __syncwarp();
-        }
-      } else {
-        float* out = static_cast<float*>(a.out_routed) + (size_t)i * a.ld_out + ti.nt * a.bn;
-        for (int c0 = 0; c0 < a.bn; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tbase + c0, v);
-          tmem_ld_wait();
-          if (valid) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) out[c0 + j] = __uint_as_float(v[j]);
+              for (int j = 0; j < 32; ++j) out[c0 + j] = __uint_as_float(v[j]);
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) aph ^= 1u;
+      if (++acc == NACC) {
+        acc = 0;
+        aph ^= 1u;
+      }
     }
   } else if (Q4) {
     // --------------------------------------------------------------- dequant
@@ -708,16 +738,16 @@ int tc_sm_count() {
 
 namespace {
 
-template <int MODE, bool Q4>
+template <int MODE, bool Q4, int RB>
 cudaError_t launch_tc(const TcMaps& maps, const TcArgs& a, int max_items, cudaStream_t st) {
-  using SP = SmemPlan<Q4>;
+  using SP = SmemPlan<Q4, RB>;
   static int attr[64] = {};
-  cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE, Q4>, (int)SP::kBytes, attr);
+  cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE, Q4, RB>, (int)SP::kBytes, attr);
   if (e != cudaSuccess) return e;
   int grid = tc_sm_count();
   if (max_items < grid) grid = max_items;
   if (grid < 1) grid = 1;
-  return launch_pdl(tc_gemm_kernel<MODE, Q4>, dim3(grid), SP::kThreadsCta, SP::kBytes, st,
+  return launch_pdl(tc_gemm_kernel<MODE, Q4, RB>, dim3(grid), SP::kThreadsCta, SP::kBytes, st,
                     maps.A0, maps.A1, maps.B0, maps.B1, maps.B2, maps.B3, a);
 }
 
@@ -750,14 +780,19 @@ bool tc_make_map_q4(CUtensorMap* m, const void* codes, uint64_t rows, uint64_t K
 
 cudaError_t launch_tc_gemm(int mode, const TcMaps& maps, const TcArgs& a, int max_items,
                            cudaStream_t st) {
+  if (mode == kTcRouter) return launch_tc<kTcRouter, false, 1>(maps, a, max_items, st);
+  if (mode != kTcGateUp && mode != kTcDown) return cudaErrorInvalidValue;
+  const bool up = mode == kTcGateUp;
   if (a.qs0) {
-    if (mode == kTcGateUp) return launch_tc<kTcGateUp, true>(maps, a, max_items, st);
-    if (mode == kTcDown) return launch_tc<kTcDown, true>(maps, a, max_items, st);
-    return cudaErrorInvalidValue;
+    if (a.pair)
+      return up ? launch_tc<kTcGateUp, true, 2>(maps, a, max_items, st)
+                : launch_tc<kTcDown, true, 2>(maps, a, max_items, st);
+    return up ? launch_tc<kTcGateUp, true, 1>(maps, a, max_items, st)
+              : launch_tc<kTcDown, true, 1>(maps, a, max_items, st);
   }
-  if (mode == kTcGateUp) return launch_tc<kTcGateUp, false>(maps, a, max_items, st);
-  if (mode == kTcDown) return launch_tc<kTcDown, false>(maps, a, max_items, st);
-  return launch_tc<kTcRouter, false>(maps, a, max_items, st);
+  if (a.pair) return cudaErrorInvalidValue;  // paired items are built for 4-bit banks only
+  return up ? launch_tc<kTcGateUp, false, 1>(maps, a, max_items, st)
+            : launch_tc<kTcDown, false, 1>(maps, a, max_items, st);
 }
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int d, void* out, int P,

@@ -349,7 +349,7 @@ def test_zero_tokens_is_a_no_op():
 # (I = 256) and two of down (d = 512), with a full fp64 oracle.
 TC_SMALL = mi.MoEShape("tc_small", 7, d_model=512, n_experts=4, top_k=2, d_ff=256,
                        d_ff_shared=256, tokens=(400,))
-PATH_CASES = [(TC_SMALL, 400), (TC_SMALL, 37), (TC_SMALL, 1), (mi.QWEN36, 64),
+PATH_CASES = [(TC_SMALL, 400), (TC_SMALL, 700), (TC_SMALL, 37), (TC_SMALL, 1), (mi.QWEN36, 64),
               (mi.DEEPSEEK_GROUP, 37)]
 
 
@@ -377,7 +377,10 @@ def test_both_expert_paths_match_oracle(shape, T, path):
 # a small full-oracle shape and the Mixtral-style layer at T=2048.
 Q4_SMALL = mi.MoEShape("q4_small", 8, d_model=512, n_experts=4, top_k=2, d_ff=256,
                        d_ff_shared=0, expert_dtype="q4", tokens=(300,))
-Q4_CASES = [(Q4_SMALL, 300, 300), (Q4_SMALL, 37, 37), (Q4_SMALL, 1, 1), (mi.MIXTRAL_Q4, 2048, 6)]
+# T=700: 350 rows per expert on average, so the 4-bit items pair row blocks
+# (with ragged pairs at every group's end)
+Q4_CASES = [(Q4_SMALL, 300, 300), (Q4_SMALL, 700, 40), (Q4_SMALL, 37, 37), (Q4_SMALL, 1, 1),
+            (mi.MIXTRAL_Q4, 2048, 6)]
 
 
 @pytest.mark.parametrize("shape,T,n_check", Q4_CASES,
