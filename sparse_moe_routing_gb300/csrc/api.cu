@@ -58,6 +58,11 @@ bool use_tc(const moe_cfg_t& c) {
   return c.path == MOE_PATH_AUTO && c.T >= kTcMinTokens;
 }
 
+// Batches of a few tokens on the GEMV path treat every (token, slot) pair
+// as its own group (at most a handful of pairs share an expert), which needs
+// no bucketing pass.
+bool gemv_pairs(const moe_cfg_t& c) { return !use_tc(c) && c.T <= kGemvSmallTokens; }
+
 // Paired GEMM items (two 128-row blocks per B tile) for 4-bit banks whose
 // routed experts average at least two row blocks each: pairing halves the
 // dequantisation per flop, which bounds those kernels (Mixtral-shape 4-bit
@@ -316,7 +321,7 @@ moe_status_t enqueue_route_bucket(const void* x, const void* W_router, const flo
                                   float* w, float* s_shared, cudaStream_t st) {
   const Plan p = make_plan(*c);
   moe_status_t s = enqueue_route(x, W_router, bias, w_shared, c, ids, w, s_shared, st);
-  if (s != MOE_OK) return s;
+  if (s != MOE_OK || gemv_pairs(*c)) return s;
   return enqueue_bucket(ids, c, at<int32_t>(c, p.counts), at<int32_t>(c, p.offsets),
                         at<int32_t>(c, p.active), &at<Ctrl>(c, 0)->n_active,
                         at<int32_t>(c, p.perm), at<int32_t>(c, p.pos), st);
@@ -426,10 +431,10 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
   return cuda_status(run(MOE_KERNEL_COMBINE, st, [&] { return launch_combine(cb, st); }));
 }
 
-moe_status_t enqueue_experts(const void* x, const float* r_attn, const float* alpha,
-                             const float* s_shared, moe_bank_t Wg, moe_bank_t Wu, moe_bank_t Wd,
-                             const void* Wsg, const void* Wsu, const void* Wsd,
-                             const moe_cfg_t* c, float* out, cudaStream_t st) {
+moe_status_t enqueue_experts(const void* x, const float* r_attn, const int32_t* ids,
+                             const float* alpha, const float* s_shared, moe_bank_t Wg,
+                             moe_bank_t Wu, moe_bank_t Wd, const void* Wsg, const void* Wsu,
+                             const void* Wsd, const moe_cfg_t* c, float* out, cudaStream_t st) {
   if (use_tc(*c))
     return enqueue_experts_tc(x, r_attn, alpha, s_shared, Wg, Wu, Wd, Wsg, Wsu, Wsd, c, out, st);
   const Plan p = make_plan(*c);
@@ -456,6 +461,11 @@ moe_status_t enqueue_experts(const void* x, const float* r_attn, const float* al
   g.I = c->d_ff; g.Is = c->d_ff_shared; g.P = c->T * c->top_k;
   g.routed_slots = g.P < g.E ? g.P : g.E;
   g.has_shared = c->d_ff_shared > 0 ? 1 : 0;
+  const bool pairs = gemv_pairs(*c);
+  if (pairs) {
+    g.pair_ids = ids;
+    g.routed_slots = g.P;
+  }
   const int act = c->act_dtype == MOE_BF16 ? 1 : 0;
   const int wdt = c->expert_dtype == MOE_F32 ? 0 : (c->expert_dtype == MOE_BF16 ? 1 : 2);
   // batches of a few tokens: one warp per weight row, direct loads; larger
@@ -469,8 +479,8 @@ moe_status_t enqueue_experts(const void* x, const float* r_attn, const float* al
     return small ? launch_gemv_small(g, act, wdt, true, st) : launch_gemv_down(g, act, wdt, st);
   });
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  CombineArgs cb{r_attn, g.Y, g.has_shared ? g.Ys : nullptr, at<int32_t>(c, p.pos), out,
-                 c->T, c->d_model, c->top_k, 0};
+  CombineArgs cb{r_attn, g.Y, g.has_shared ? g.Ys : nullptr,
+                 pairs ? nullptr : at<int32_t>(c, p.pos), out, c->T, c->d_model, c->top_k, 0};
   return cuda_status(run(MOE_KERNEL_COMBINE, st, [&] { return launch_combine(cb, st); }));
 }
 
@@ -617,12 +627,14 @@ moe_status_t moe_experts_forward(const void* x, const float* r_attn, const int32
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     s_shared = at<float>(cfg, p.s_shared);
   }
-  s = enqueue_bucket(topk_ids, cfg, at<int32_t>(cfg, p.counts), at<int32_t>(cfg, p.offsets),
-                     at<int32_t>(cfg, p.active), &at<Ctrl>(cfg, 0)->n_active,
-                     at<int32_t>(cfg, p.perm), at<int32_t>(cfg, p.pos), st);
-  if (s != MOE_OK) return s;
-  return enqueue_experts(x, r_attn, weights, s_shared, W_gate, W_up, W_down, Ws_gate, Ws_up,
-                         Ws_down, cfg, out, st);
+  if (!gemv_pairs(*cfg)) {
+    s = enqueue_bucket(topk_ids, cfg, at<int32_t>(cfg, p.counts), at<int32_t>(cfg, p.offsets),
+                       at<int32_t>(cfg, p.active), &at<Ctrl>(cfg, 0)->n_active,
+                       at<int32_t>(cfg, p.perm), at<int32_t>(cfg, p.pos), st);
+    if (s != MOE_OK) return s;
+  }
+  return enqueue_experts(x, r_attn, topk_ids, weights, s_shared, W_gate, W_up, W_down, Ws_gate,
+                         Ws_up, Ws_down, cfg, out, st);
 }
 
 moe_status_t moe_layer_forward(const void* x, const float* r_attn, const void* W_router,
@@ -654,8 +666,8 @@ moe_status_t moe_layer_forward(const void* x, const float* r_attn, const void* W
   s = enqueue_route_bucket(x, W_router, expert_bias, shared ? w_shared : nullptr, cfg, topk_ids,
                            weights, s_sh, st);
   if (s != MOE_OK) return s;
-  return enqueue_experts(x, r_attn, weights, s_sh, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
-                         cfg, out, st);
+  return enqueue_experts(x, r_attn, topk_ids, weights, s_sh, W_gate, W_up, W_down, Ws_gate, Ws_up,
+                         Ws_down, cfg, out, st);
 }
 
 }  // extern "C"

@@ -19,7 +19,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   pdl_trigger();
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s = 0; s < a.k; ++s) {
-    const int p = a.pos[(size_t)t * a.k + s];
+    const int p = a.pos ? a.pos[(size_t)t * a.k + s] : t * a.k + s;
     const float4 y = reinterpret_cast<const float4*>(a.Y + (size_t)p * a.d)[c];
     acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
   }
@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(CombineArgs a) {
   const __nv_bfloat16* Ys = reinterpret_cast<const __nv_bfloat16*>(a.Ys);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s = 0; s < a.k; ++s) {
-    const int p = a.pos[(size_t)t * a.k + s];
+    const int p = a.pos ? a.pos[(size_t)t * a.k + s] : t * a.k + s;
     add_bf16x4(acc, Y + (size_t)p * a.d + c * 4);
   }
   if (Ys) add_bf16x4(acc, Ys + (size_t)t * a.d + c * 4);

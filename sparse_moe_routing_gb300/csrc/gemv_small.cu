@@ -26,9 +26,22 @@ struct SGroup {
   int g, n, row0, width;
 };
 
-// Group slot -> routed expert (active list order) or the shared expert.
+// Group slot -> routed expert (active list order; or, in pair mode, the
+// pair's expert) or the shared expert.
 __device__ __forceinline__ SGroup group_at(const GemvArgs& a, int slot) {
   SGroup v{};
+  if (a.pair_ids && slot < a.routed_slots) {
+    v.g = a.pair_ids[slot];
+    if (v.g < 0 || v.g >= a.E) {
+      if (threadIdx.x == 0) report(a.ctrl, kDevBadId, kSiteGemvGateUp);
+      return v;
+    }
+    v.row0 = slot;
+    v.n = 1;
+    v.width = a.I;
+    v.ok = true;
+    return v;
+  }
   if (slot < a.routed_slots) {
     if (slot >= *a.n_active) return v;
     v.g = a.active[slot];
@@ -59,7 +72,8 @@ __device__ __forceinline__ void gateup_rows(const GemvArgs& a, const SGroup& v, 
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
     const int i = j0 + j;
-    const int tok = j < nj ? (v.shared ? i : a.perm[v.row0 + i] / a.k) : 0;
+    int tok = 0;
+    if (j < nj) tok = v.shared ? i : (a.pair_ids ? v.row0 + i : a.perm[v.row0 + i]) / a.k;
     xr[j] = reinterpret_cast<const uint4*>(static_cast<const TW*>(a.x) + (size_t)tok * a.d);
   }
   constexpr int NV = P2<2 * NT>::v;
@@ -169,7 +183,8 @@ __device__ __forceinline__ void down_rows(const GemvArgs& a, const SGroup& v, in
     const int r = idx / NT, j = idx - r * NT;
     if (r < nr && j < nj) {
       const int i = j0 + j;
-      const float scale = v.shared ? a.s_shared[i] : a.alpha[a.perm[v.row0 + i]];
+      const float scale = v.shared ? a.s_shared[i]
+                                   : a.alpha[a.pair_ids ? v.row0 + i : a.perm[v.row0 + i]];
       float* Y = v.shared ? a.Ys + (size_t)i * a.d : a.Y + (size_t)(v.row0 + i) * a.d;
       Y[col0 + r] = scale * sum;
     }

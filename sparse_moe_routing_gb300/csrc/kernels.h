@@ -69,13 +69,17 @@ struct GemvArgs {
   int T, d, E, k, I, Is, P;
   int routed_slots;         // grid.y entries for routed groups (= min(E, P))
   int has_shared;
+  // direct-load GEMV only: when set, every routed (token, slot) pair is its
+  // own group (expert ids[p], one token p / k, packed row p), so no
+  // bucketing pass is needed; routed_slots = P
+  const int32_t* pair_ids;
 };
 
 struct CombineArgs {
   const float* r_attn;      // [T][d]
   const float* Y;           // [P][d] f32, or bf16 when y_bf16
   const float* Ys;          // [T][d] or null (same dtype as Y)
-  const int32_t* pos;       // [P]
+  const int32_t* pos;       // [P], or null: pair p at row p
   float* out;               // [T][d]
   int T, d, k;
   int y_bf16;

@@ -23,17 +23,18 @@
 
 namespace moe {
 
-// Dot products of one router row with up to KTOK consecutive tokens (x rows
-// d elements apart), by one whole warp; afterwards every lane holds the sums
-// acc[t] for t < nt.
+// Dot products of one router row with up to KTOK tokens whose activation
+// rows (nvec 16-byte chunks each, consecutive) start at xr (shared or global
+// memory), by one whole warp; afterwards every lane holds the sums acc[t] for
+// t < nt. kU weight chunks per lane are held in registers while the tokens
+// stream past.
 template <typename TA, int KTOK>
-__device__ __forceinline__ void router_row_dots(const TA* wrow, const TA* x, int d, int nt,
+__device__ __forceinline__ void router_row_dots(const TA* wrow, const uint4* xr, int nvec, int nt,
                                                 int lane, float* acc) {
   constexpr int kVec = Chunk<TA>::kVec;
-  constexpr int kU = 8;  // weight chunks per lane held while the tokens stream past
+  constexpr int kU = 8;
 #pragma unroll
   for (int t = 0; t < KTOK; ++t) acc[t] = 0.f;
-  const int nvec = d / kVec;
   for (int c0 = lane; c0 < nvec; c0 += 32 * kU) {
     float w[kU][kVec];
 #pragma unroll
@@ -45,12 +46,12 @@ __device__ __forceinline__ void router_row_dots(const TA* wrow, const TA* x, int
 #pragma unroll
     for (int t = 0; t < KTOK; ++t) {
       if (t < nt) {
-        const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+        const uint4* xt = xr + (size_t)t * nvec;
         uint4 xv[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
           const int c = c0 + 32 * u;
-          xv[u] = c < nvec ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+          xv[u] = c < nvec ? xt[c] : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
@@ -269,16 +270,6 @@ __device__ __forceinline__ void topk_token_pl(const TopkArgs& a, int t, int lane
   }
   if (lane == 0 && a.s_shared && a.has_shared_logit)
     a.s_shared[t] = 1.0f / (1.0f + expf(-__ldcg(z + E)));
-}
-
-// The routing rule for token t (E <= 512), with the per-lane slot count
-// chosen from E.
-__device__ __forceinline__ void topk_token(const TopkArgs& a, int t, int lane) {
-  if (a.E <= 32) topk_token_pl<1>(a, t, lane);
-  else if (a.E <= 64) topk_token_pl<2>(a, t, lane);
-  else if (a.E <= 128) topk_token_pl<4>(a, t, lane);
-  else if (a.E <= 256) topk_token_pl<8>(a, t, lane);
-  else topk_token_pl<16>(a, t, lane);
 }
 
 }  // namespace moe

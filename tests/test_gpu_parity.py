@@ -231,6 +231,29 @@ def test_small_gemv_with_an_expert_repeated_within_a_token(shape, T):
     assert rel_rms_err(dev.out.cpu().numpy(), ref["out"]) <= OUT_TOL[shape.act_dtype]
 
 
+def test_few_token_gemv_flags_out_of_range_ids():
+    """Batches of a few tokens skip the bucketing pass (each pair is its own
+    group), so the GEMV kernels check the ids themselves: a bad id is flagged
+    in the status word and its pair is skipped, with every access in bounds."""
+    shape, T = mi.QWEN36, 2
+    L = layer_host(shape, T)
+    dev = DevLayer(shape, L)
+    ids, w, s = mi.random_router_outputs(shape, T)
+    ids[1, 3] = shape.n_experts + 7
+    cfg = cfg_for(shape, T)
+    ws = smr.alloc_workspace(cfg)
+    smr.experts_forward(cfg, ws, dev.t["x"], dev.t["r_attn"], to_dev(ids), to_dev(w),
+                        dev.bank("W_gate"), dev.bank("W_up"), dev.bank("W_down"), dev.out,
+                        s_shared=to_dev(s), **dev.shared())
+    st, word = smr.read_device_status(cfg, ws)
+    assert st == smr._STATUS.index("MOE_ERR_DEVICE_CHECK")
+    assert word & 1 and (word >> 16) == 2
+    # token 0 does not involve the bad pair and is still exact
+    ref = orc.moe_experts_forward(L, shape, ids[:1], w[:1].astype(np.float64),
+                                  s[:1].astype(np.float64), np.arange(1))
+    assert rel_rms_err(dev.out.cpu().numpy()[:1], ref["out"]) <= OUT_TOL[shape.act_dtype]
+
+
 def test_in_place_residual_update():
     shape, T = mi.QWEN36, 8
     L = layer_host(shape, T)
