@@ -44,7 +44,7 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s (Qwen3.6 shape, T=1..4096); % of HBM/tensor roofline"
 L2_BYTES = 129 * 10 ** 6
-TC_MIN_TOKENS = 4  # the library's MOE_PATH_AUTO switch to the tensor-core path
+TC_MIN_TOKENS = 6  # the library's MOE_PATH_AUTO switch to the tensor-core path
 
 WORKLOADS = {
     # name: (preset, default T, description)

@@ -104,8 +104,9 @@ typedef enum {
 
 /* Expert-path selection for moe_layer_forward / moe_experts_forward. */
 typedef enum {
-  MOE_PATH_AUTO = 0,   /* by shape: streaming GEMV for small T, tensor-core
-                          grouped GEMM for large T (bf16/q4 experts only) */
+  MOE_PATH_AUTO = 0,   /* by shape: CUDA-core GEMV for T <= 5, tensor-core
+                          grouped GEMM for T >= 6 (bf16 experts; 4-bit
+                          experts always take the tensor-core path) */
   MOE_PATH_GEMV = 1,   /* CUDA-core weight-streaming GEMV at any T */
   MOE_PATH_TC = 2      /* tcgen05 grouped GEMM (bf16/q4 experts only) */
 } moe_path_t;

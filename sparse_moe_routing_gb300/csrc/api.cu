@@ -23,8 +23,10 @@ struct Plan {
 };
 
 // Token batches at or above this size take the tensor-core path under
-// MOE_PATH_AUTO (when the shape allows it).
-constexpr int kTcMinTokens = 4;
+// MOE_PATH_AUTO (when the shape allows it). Measured per layer at the Qwen3.6
+// shape (direct-load GEMV / tensor cores): T=4 57 / 68 us, T=5 83 / 89 us,
+// T=6 96 / 92 us, T=8 123 / 100 us.
+constexpr int kTcMinTokens = 6;
 
 // The tensor-core path: bf16 experts and activations, K dims multiples of the
 // 64-element TMA box, N tiles of 128 (gate/up) and 256 (down), and a shared

@@ -3,7 +3,7 @@
 // MoE tokens", "Routed expert computation" and "Shared expert computation";
 // Edge0 "Experts").
 //
-// With one to four tokens an expert sees at most that many tokens, so each
+// With a few tokens an expert sees at most that many tokens, so each
 // weight row feeds one dot product per token and the layer is a pure weight
 // stream. Here one warp owns one gate/up row pair (or four down rows) and
 // streams it with 16-byte no-allocate loads, kUnroll chunks per lane in
@@ -224,13 +224,13 @@ cudaError_t launch_small(const GemvArgs& a, bool down, cudaStream_t st) {
 
 template <typename TW>
 cudaError_t dispatch(const GemvArgs& a, bool down, cudaStream_t st) {
-  switch (a.T) {
-    case 1: return launch_small<TW, 1>(a, down, st);
-    case 2: return launch_small<TW, 2>(a, down, st);
-    case 3: return launch_small<TW, 3>(a, down, st);
-    case 4: return launch_small<TW, 4>(a, down, st);
-    default: return cudaErrorInvalidValue;
-  }
+  // tokens per pass: the batch rounded up to a power of two (a routed pair
+  // group holds one token; the shared expert holds all T)
+  if (a.T <= 1) return launch_small<TW, 1>(a, down, st);
+  if (a.T <= 2) return launch_small<TW, 2>(a, down, st);
+  if (a.T <= 4) return launch_small<TW, 4>(a, down, st);
+  if (a.T <= 8) return launch_small<TW, 8>(a, down, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace

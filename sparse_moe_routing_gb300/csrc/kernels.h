@@ -186,7 +186,7 @@ cudaError_t launch_gemv_gateup(const GemvArgs& a, int act, int wdt, cudaStream_t
 cudaError_t launch_gemv_down(const GemvArgs& a, int act, int wdt, cudaStream_t st);
 // Direct-load GEMV for batches of at most kGemvSmallTokens tokens
 // (gemv_small.cu): down = false runs gate/up + SwiGLU, true runs down x alpha.
-constexpr int kGemvSmallTokens = 4;
+constexpr int kGemvSmallTokens = 8;
 cudaError_t launch_gemv_small(const GemvArgs& a, int act, int wdt, bool down, cudaStream_t st);
 // True when the GEMV kernels can stage at least one token of width d and kmax.
 bool gemv_supported(int d, int kmax);

@@ -373,6 +373,7 @@ def test_zero_tokens_is_a_no_op():
 TC_SMALL = mi.MoEShape("tc_small", 7, d_model=512, n_experts=4, top_k=2, d_ff=256,
                        d_ff_shared=256, tokens=(400,))
 PATH_CASES = [(TC_SMALL, 400), (TC_SMALL, 700), (TC_SMALL, 37), (TC_SMALL, 1), (mi.QWEN36, 64),
+              (mi.QWEN36, 8), (mi.QWEN36, 5), (mi.DEEPSEEK_GROUP, 6),
               (mi.DEEPSEEK_GROUP, 37)]
 
 
