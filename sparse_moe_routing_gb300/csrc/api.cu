@@ -370,11 +370,16 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
     return q4 ? tc_make_map_q4(mp, w, rows, K, box) : tc_make_map(mp, w, rows, K, box);
   };
   // gate/up: A = X_perm (routed) / x (shared), B = gate and up rows (4-bit
-  // codes for q4 banks, dequantised in the kernel)
+  // codes for q4 banks, dequantised in the kernel). N tile = bn/2 gate + bn/2
+  // up columns: 128 + 128, or 64 + 64 when the bf16 work list is too short
+  // for 4 waves of 256-wide items (decode batches: finer items even out the
+  // last wave of the weight stream)
+  const int gu_bn = (!q4 && (long long)max_rb * (I / 128) < 4LL * tc_sm_count()) ? 128 : 256;
+  const uint32_t gu_rows = gu_bn / 2;
   TcMaps m{};
   bool ok = tc_make_map(&m.A0, xperm, P, d, 128) && tc_make_map(&m.A1, x, T, d, 128) &&
-            bmap(&m.B0, Wg.w, (uint64_t)E * I, d, 128) &&
-            bmap(&m.B1, Wu.w, (uint64_t)E * I, d, 128);
+            bmap(&m.B0, Wg.w, (uint64_t)E * I, d, gu_rows) &&
+            bmap(&m.B1, Wu.w, (uint64_t)E * I, d, gu_rows);
   if (q4) {
     a.qs0 = static_cast<const __nv_bfloat16*>(Wg.scale);
     a.qm0 = static_cast<const __nv_bfloat16*>(Wg.minv);
@@ -382,7 +387,8 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
     a.qm1 = static_cast<const __nv_bfloat16*>(Wu.minv);
     a.qgroups = d / 64;
   }
-  if (ok && shared) ok = tc_make_map(&m.B2, Wsg, Is, d, 128) && tc_make_map(&m.B3, Wsu, Is, d, 128);
+  if (ok && shared)
+    ok = tc_make_map(&m.B2, Wsg, Is, d, gu_rows) && tc_make_map(&m.B3, Wsu, Is, d, gu_rows);
   if (!ok) return MOE_ERR_CUDA;
   if (!shared) {
     m.B2 = m.B0;
@@ -392,8 +398,8 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
   a.out_shared = Hs;
   a.K = d;
   a.ld_out = I;
-  a.n_tiles = I / 128;
-  a.bn = 256;
+  a.n_tiles = I / gu_rows;
+  a.bn = gu_bn;
   a.brows_routed = I;
   e = run(MOE_KERNEL_TC_GATEUP, st,
           [&] { return launch_tc_gemm(kTcGateUp, m, a, max_rb * a.n_tiles, st); });
