@@ -455,6 +455,8 @@ def run_ours(args):
     T = args.tokens or T_default
     weights = Weights(shape, device)
 
+    load = {}
+
     def measure(T, main):
         """The timed replay (no event nodes inside the graph); for the main
         workload also the clocks during it and, from one more replay with
@@ -466,7 +468,14 @@ def run_ours(args):
         sampler = ClockSampler(local) if main else None
         ms, launches, _, (t0, t1) = time_graph(wl, K, W, None, sampler)
         durs = time_graph(wl, min(K, 100), 3, kern)[2] if main else []
-        n_act = int(np.unique(wl.ids.cpu().numpy()).size)
+        ids = wl.ids.cpu().numpy().ravel()
+        n_act = int(np.unique(ids).size)
+        if main:
+            # load histogram of the routed pairs over the experts
+            cnt = np.bincount(ids, minlength=shape.n_experts)
+            load["expert_rows_max"] = int(cnt.max())
+            load["expert_rows_mean_active"] = float(cnt[cnt > 0].mean())
+            load["idle_experts"] = int((cnt == 0).sum())
         clocks = sampler.summary(t0, t1) if sampler else None
         return wl, ms, launches, durs, n_act, clocks, kern
 
@@ -508,7 +517,7 @@ def run_ours(args):
                         "kernel's mean duration from a second replay with it bracketed by "
                         "in-graph events",
               "parallelism": "replicas" if world == 1 else "dp%d (independent replicas)" % world,
-              "active_experts": n_act, "layer_alg_bytes": lb, "layer_alg_flops": lf,
+              "active_experts": n_act, **load, "layer_alg_bytes": lb, "layer_alg_flops": lf,
               "layer_hbm_frac": lb / (ms_step * 1e-3) / 1e9 / hbm,
               "layer_tensor_frac": lf / (ms_step * 1e-3) / 1e12 / tflops})
     if not args.no_sweep and args.workload == "decode":

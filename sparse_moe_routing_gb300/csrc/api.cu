@@ -7,6 +7,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -185,8 +187,31 @@ cudaError_t trace_record(cudaEvent_t ev, cudaStream_t st) {
   return cudaEventRecord(ev, st);
 }
 
+// NVTX range names per kernel family (host-side ranges around each launch,
+// visible to nsys / ncu --nvtx; free when no tool is attached).
+const char* kernel_name(int kid) {
+  switch (kid) {
+    case MOE_KERNEL_ROUTER_LOGITS: return "moe:router_logits";
+    case MOE_KERNEL_ROUTER_TOPK: return "moe:router_topk";
+    case MOE_KERNEL_SHARED_GATE: return "moe:shared_gate";
+    case MOE_KERNEL_BUCKET: return "moe:bucket";
+    case MOE_KERNEL_GEMV_GATEUP: return "moe:gemv_gateup";
+    case MOE_KERNEL_GEMV_DOWN: return "moe:gemv_down";
+    case MOE_KERNEL_COMBINE: return "moe:combine";
+    case MOE_KERNEL_TC_GATEUP: return "moe:tc_gateup";
+    case MOE_KERNEL_TC_DOWN: return "moe:tc_down";
+    case MOE_KERNEL_GATHER: return "moe:gather";
+    case MOE_KERNEL_TC_ROUTER: return "moe:tc_router";
+  }
+  return "moe:kernel";
+}
+
 template <typename F>
 cudaError_t run(int kid, cudaStream_t st, F&& launch) {
+  struct Range {
+    explicit Range(const char* n) { nvtxRangePushA(n); }
+    ~Range() { nvtxRangePop(); }
+  } range(kernel_name(kid));
   const bool tr = g_trace.kernel == kid && g_trace.n > 0;
   const int slot = tr ? (*g_trace.count % g_trace.n) : 0;
   if (tr && trace_record(g_trace.starts[slot], st) != cudaSuccess) return cudaErrorUnknown;
