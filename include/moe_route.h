@@ -108,7 +108,11 @@ typedef enum {
                           grouped GEMM for T >= 6 (bf16 experts; 4-bit
                           experts always take the tensor-core path) */
   MOE_PATH_GEMV = 1,   /* CUDA-core weight-streaming GEMV at any T */
-  MOE_PATH_TC = 2      /* tcgen05 grouped GEMM (bf16/q4 experts only) */
+  MOE_PATH_TC = 2      /* tcgen05 grouped GEMM: bf16 or 4-bit experts with bf16
+                          activations, d_model % 256 == 0, d_ff % 128 == 0,
+                          d_ff_shared 0 or == d_ff (4-bit: 0); other shapes
+                          return MOE_ERR_UNSUPPORTED (and MOE_PATH_AUTO then
+                          uses the GEMV path) */
 } moe_path_t;
 
 typedef struct {
@@ -143,9 +147,9 @@ typedef enum {
   MOE_KERNEL_ROUTER_LOGITS = 1, /* router contraction (+ shared-gate logit) */
   MOE_KERNEL_ROUTER_TOPK = 2,   /* routing rule, one warp per token */
   MOE_KERNEL_SHARED_GATE = 3,   /* shared gate alone (moe_experts_forward) */
-  MOE_KERNEL_BUCKET = 4,        /* counting and packing pass */
-  MOE_KERNEL_GEMV_GATEUP = 5,   /* streaming gate/up + SwiGLU */
-  MOE_KERNEL_GEMV_DOWN = 6,     /* streaming down x alpha */
+  MOE_KERNEL_BUCKET = 4,        /* counting and packing pass (1 or 2 launches) */
+  MOE_KERNEL_GEMV_GATEUP = 5,   /* CUDA-core gate/up + SwiGLU (direct-load or streaming) */
+  MOE_KERNEL_GEMV_DOWN = 6,     /* CUDA-core down x alpha (direct-load or streaming) */
   MOE_KERNEL_COMBINE = 7,       /* unpermute, shared branch, residual */
   MOE_KERNEL_TC_GATEUP = 8,     /* tensor-core grouped gate/up + SwiGLU */
   MOE_KERNEL_TC_DOWN = 9,       /* tensor-core grouped down x alpha */
@@ -238,7 +242,10 @@ MOE_API moe_status_t moe_bucket(const int32_t* topk_ids, const moe_cfg_t* cfg,
  * "Shared expert computation", the residual add of "Pseudocode"):
  * out = r_attn + sum_slot weights * expert(x) + s_shared * shared(x).
  * s_shared [T] f32 may be NULL, in which case the gate is computed from
- * w_shared; both NULL is invalid when d_ff_shared > 0. */
+ * w_shared; both NULL is invalid when d_ff_shared > 0. Ids outside [0, E)
+ * are flagged in the status word (MOE_ERR_DEVICE_CHECK from
+ * moe_read_device_status) and every access stays in bounds; the outputs of
+ * the tokens involved are then unspecified. */
 MOE_API moe_status_t moe_experts_forward(const void* x, const float* r_attn,
                                  const int32_t* topk_ids, const float* weights,
                                  const float* s_shared,
