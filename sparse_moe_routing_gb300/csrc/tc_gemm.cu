@@ -216,16 +216,17 @@ constexpr int kDequantWarps = 8;
 // stages of A + B. 4-bit: kStages stages of A + raw codes (filled by TMA,
 // freed by the MMA) and kBStages dequantised B stages (filled by the
 // dequant warps, freed by the MMA), so the copies run further ahead than
-// 48 KB stages would allow.
+// 48 KB stages would allow. EPI: the down epilogue's staging rows (the other
+// modes leave that shared memory to the pipeline).
 //
 // RB = row blocks per work item. RB = 2 ("paired" items, used for 4-bit
 // banks): two 128-row blocks of one group share each B stage (two A tiles
 // per stage, two MMAs per k-block into two 256-column accumulators that fill
 // TMEM), halving the B traffic and the dequantisation per flop; the
 // accumulator is then single-buffered.
-template <bool Q4, int RB>
+template <bool Q4, int RB, bool EPI>
 struct SmemPlan {
-  static constexpr int kStages = RB == 2 ? 3 : (Q4 ? 5 : 4);
+  static constexpr int kStages = RB == 2 ? (EPI ? 3 : 4) : (Q4 ? 5 : 4);
   static constexpr int kBStages = Q4 ? 2 : kStages;
   static constexpr int kNAcc = 2 / RB;   // accumulator buffers of RB x 256 TMEM columns
   static constexpr int kStageQ = 256 * (BK / 2);  // raw 4-bit codes of one B stage
@@ -234,8 +235,9 @@ struct SmemPlan {
   static constexpr size_t kB = kA + (size_t)kStages * RB * kStageA;
   static constexpr size_t kQ = kB + (size_t)kBStages * kStageB;
   static constexpr size_t kEpi = kQ + (Q4 ? (size_t)kStages * kStageQ : 0);
-  static constexpr size_t kBars = kEpi + 4 * (size_t)kEpiWarpBytes;
+  static constexpr size_t kBars = kEpi + (EPI ? 4 * (size_t)kEpiWarpBytes : 0);
   static constexpr size_t kBytes = 1024 + kBars + 256;
+  static_assert(kBytes <= 227 * 1024, "shared memory plan exceeds 227 KB");
 };
 
 // The (scale, min) arrays of the B row a dequant thread owns: bank row and
@@ -305,12 +307,12 @@ __device__ __forceinline__ void dequant_row(const uint8_t* q_row_src, uint8_t* b
 }
 
 template <int MODE, bool Q4, int RB>
-__global__ void __launch_bounds__(SmemPlan<Q4, RB>::kThreadsCta, 1)
+__global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown>::kThreadsCta, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmB3,
                    const TcArgs a) {
-  using SP = SmemPlan<Q4, RB>;
+  using SP = SmemPlan<Q4, RB, MODE == kTcDown>;
   constexpr int STAGES = SP::kStages;
   constexpr int NACC = SP::kNAcc;
   extern __shared__ uint8_t smem_raw[];
@@ -679,22 +681,6 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB>::kThreadsCta, 1)
 }
 
 // ---------------------------------------------------------------------------
-// X_perm[p] = x[perm[p] / k] (rows of the packed order, bf16)
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
-                                                          const int32_t* __restrict__ perm, int k,
-                                                          int row_vecs, uint4* __restrict__ out,
-                                                          int P) {
-  pdl_wait();
-  pdl_trigger();
-  for (int p = blockIdx.x; p < P; p += gridDim.x) {
-    const size_t src = (size_t)(perm[p] / k) * row_vecs;
-    const size_t dst = (size_t)p * row_vecs;
-    for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) out[dst + v] = __ldg(x + src + v);
-  }
-}
-
-// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -740,7 +726,7 @@ namespace {
 
 template <int MODE, bool Q4, int RB>
 cudaError_t launch_tc(const TcMaps& maps, const TcArgs& a, int max_items, cudaStream_t st) {
-  using SP = SmemPlan<Q4, RB>;
+  using SP = SmemPlan<Q4, RB, MODE == kTcDown>;
   static int attr[64] = {};
   cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE, Q4, RB>, (int)SP::kBytes, attr);
   if (e != cudaSuccess) return e;
@@ -793,14 +779,6 @@ cudaError_t launch_tc_gemm(int mode, const TcMaps& maps, const TcArgs& a, int ma
   if (a.pair) return cudaErrorInvalidValue;  // paired items are built for 4-bit banks only
   return up ? launch_tc<kTcGateUp, false, 1>(maps, a, max_items, st)
             : launch_tc<kTcDown, false, 1>(maps, a, max_items, st);
-}
-
-cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int d, void* out, int P,
-                               cudaStream_t st) {
-  if (P == 0) return cudaSuccess;
-  int grid = P < tc_sm_count() * 16 ? P : tc_sm_count() * 16;
-  return launch_pdl(gather_rows_kernel, dim3(grid), 256, 0, st, static_cast<const uint4*>(x),
-                    perm, k, d / 8, static_cast<uint4*>(out), P);
 }
 
 }  // namespace moe
