@@ -487,18 +487,11 @@ def run_ours(args):
     # roofline of the dominant kernel: bytes and flops per launch, bound by
     # whichever floor is larger
     mean_k = sum(durs) / len(durs) if durs else None
-    gb, gf = gateup_work(shape, T, n_active=n_act)
+    gb, gf = gateup_work(shape, T, n_act)
     hbm_bound = gb / (hbm * 1e9) >= gf / (tflops * 1e12)
-    # gate/up weights of active experts that the router kernel prefetched into
-    # L2 during routing: the gate/up kernel does not stream them from HBM, so
-    # its achieved HBM rate leaves them out
-    per_expert = 2 * shape.d_ff * shape.d_model * _wbytes(shape)
-    n_pf = smr.layer_l2_prefetch_bytes(wl.cfg) // int(per_expert)
-    ids_np = wl.ids.cpu().numpy().ravel()
-    pf_active = int(np.unique(ids_np[ids_np < n_pf]).size * per_expert)
     if mean_k:
         sec = mean_k * 1e-3
-        ach = (gb - pf_active) / sec / 1e9 if hbm_bound else gf / sec / 1e12
+        ach = gb / sec / 1e9 if hbm_bound else gf / sec / 1e12
     else:
         ach = None
     peak = hbm if hbm_bound else tflops
@@ -510,7 +503,6 @@ def run_ours(args):
                 "traffic": (tr["dram_bytes_per_unit"] * (n_act + (1 if shape.d_ff_shared else 0))
                             if tr else None),
                 "peak_source": peak_src, "algorithmic_bytes_per_launch": gb,
-                "l2_prefetched_bytes": pf_active,
                 "algorithmic_flops_per_launch": gf,
                 "units_per_launch": n_act + (1 if shape.d_ff_shared else 0),
                 "mean_launch_us": mean_k * 1e3 if mean_k else None}

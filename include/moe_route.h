@@ -144,9 +144,7 @@ typedef struct {
 
 /* Kernel families launched by this library (for moe_trace_kernel). */
 typedef enum {
-  MOE_KERNEL_ROUTER_LOGITS = 1, /* router contraction (+ shared-gate logit; in moe_layer_forward at
-                                   decode sizes also an L2 prefetch of the first experts' gate/up
-                                   weights) */
+  MOE_KERNEL_ROUTER_LOGITS = 1, /* router contraction (+ shared-gate logit) */
   MOE_KERNEL_ROUTER_TOPK = 2,   /* routing rule, one warp per token */
   MOE_KERNEL_SHARED_GATE = 3,   /* shared gate alone (moe_experts_forward) */
   MOE_KERNEL_BUCKET = 4,        /* counting and packing pass (1 or 2 launches) */
@@ -187,15 +185,6 @@ MOE_API moe_status_t moe_trace_kernel(int kernel, void* const* starts, void* con
 /* Workspace bytes needed by every call below for this cfg (the workspace
  * fields of cfg are ignored). Returns 0 if cfg is invalid. */
 MOE_API size_t moe_workspace_bytes(const moe_cfg_t* cfg);
-
-/* Bytes of expert weights (gate and up banks together) that
- * moe_layer_forward with this cfg bulk-prefetches into L2 while it routes:
- * the first experts' gate and up rows, taken in expert-id order, within a
- * 32 MB budget. Non-zero only for bf16 banks on the tensor-core path with
- * T <= 128, T*k >= 2E and the router on CUDA cores (T < 128, or E not a
- * multiple of 32);
- * 0 otherwise or if cfg is invalid. The prefetch changes no result. */
-MOE_API size_t moe_layer_l2_prefetch_bytes(const moe_cfg_t* cfg);
 
 /* Zeroes the workspace's control words (status word and counters). Must be
  * enqueued once on a freshly allocated workspace before its first use. */

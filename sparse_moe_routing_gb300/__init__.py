@@ -63,7 +63,6 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(_Cfg)]),
     "moe_workspace_init": (ctypes.c_int, [ctypes.POINTER(_Cfg), _P]),
-    "moe_layer_l2_prefetch_bytes": (ctypes.c_size_t, [ctypes.POINTER(_Cfg)]),
     "moe_read_device_status": (ctypes.c_int, [ctypes.POINTER(_Cfg), _P,
                                               ctypes.POINTER(ctypes.c_uint32)]),
     "moe_route": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(_Cfg), _P, _P, _P, _P]),
@@ -174,11 +173,6 @@ def workspace_bytes(cfg: MoEConfig) -> int:
     if n == 0:
         raise MoEError(1, "moe_workspace_bytes")
     return n
-
-
-def layer_l2_prefetch_bytes(cfg: MoEConfig) -> int:
-    """Expert-weight bytes layer_forward prefetches into L2 while routing."""
-    return int(lib().moe_layer_l2_prefetch_bytes(ctypes.byref(cfg._c())))
 
 
 def alloc_workspace(cfg: MoEConfig, device=None, stream=None):

@@ -78,36 +78,6 @@ bool use_pair(const moe_cfg_t& c) {
          (long long)c.T * c.top_k >= 2LL * kTcBm * c.n_experts;
 }
 
-// L2 prefetch of the first experts' gate and up weights, issued by extra CTAs
-// of the CUDA-core router kernel. It applies to decode-sized batches on the
-// tensor-core path (T <= 128, so every group fits one row block and the
-// gate/up kernel takes the active experts in id order) where most experts are
-// active (T k >= 2E). The router, routing rule, bucketing and gather kernels
-// leave HBM nearly idle; meanwhile the lowest-id experts' weights, which the
-// gate/up kernel's first wave reads, are brought into L2.
-#ifndef MOE_L2_PREFETCH_MB
-#define MOE_L2_PREFETCH_MB 32
-#endif
-struct L2Prefetch {
-  const void* gate = nullptr;
-  const void* up = nullptr;
-  unsigned long long bytes = 0;  // per bank
-};
-
-L2Prefetch l2_prefetch_plan(const moe_cfg_t& c, const moe_bank_t& Wg, const moe_bank_t& Wu) {
-  L2Prefetch pf;
-  if (MOE_L2_PREFETCH_MB <= 0 || !use_tc(c) || use_tc_router(c) || c.expert_dtype != MOE_BF16 ||
-      c.T > kTcBm || (long long)c.T * c.top_k < 2LL * c.n_experts)
-    return pf;
-  const unsigned long long per_bank = (unsigned long long)c.d_ff * c.d_model * 2;  // one expert
-  unsigned long long n = (unsigned long long)MOE_L2_PREFETCH_MB * (1ull << 20) / (2 * per_bank);
-  if (n > (unsigned long long)c.n_experts) n = c.n_experts;
-  pf.gate = Wg.w;
-  pf.up = Wu.w;
-  pf.bytes = n * per_bank;
-  return pf;
-}
-
 Plan make_plan(const moe_cfg_t& c) {
   Plan p{};
   size_t off = 0;
@@ -293,11 +263,8 @@ TopkArgs topk_args(const RouterArgs& ra, const float* bias, const moe_cfg_t* c, 
 
 moe_status_t enqueue_route(const void* x, const void* W_router, const float* bias,
                            const void* w_shared, const moe_cfg_t* c, int32_t* ids, float* w,
-                           float* s_shared, cudaStream_t st, const L2Prefetch& pf = {}) {
-  RouterArgs ra = router_args(x, W_router, w_shared, c, s_shared);
-  ra.pf0 = pf.gate;
-  ra.pf1 = pf.up;
-  ra.pf_bytes = pf.bytes;
+                           float* s_shared, cudaStream_t st) {
+  const RouterArgs ra = router_args(x, W_router, w_shared, c, s_shared);
   TopkArgs ta = topk_args(ra, bias, c, ids, w, s_shared);
   const bool bf16 = c->act_dtype == MOE_BF16;
   cudaError_t e;
@@ -378,10 +345,9 @@ moe_status_t enqueue_bucket(const int32_t* ids, const moe_cfg_t* c, int32_t* cou
 // Routing and bucketing of the layer's own batch.
 moe_status_t enqueue_route_bucket(const void* x, const void* W_router, const float* bias,
                                   const void* w_shared, const moe_cfg_t* c, int32_t* ids,
-                                  float* w, float* s_shared, cudaStream_t st,
-                                  const L2Prefetch& pf = {}) {
+                                  float* w, float* s_shared, cudaStream_t st) {
   const Plan p = make_plan(*c);
-  moe_status_t s = enqueue_route(x, W_router, bias, w_shared, c, ids, w, s_shared, st, pf);
+  moe_status_t s = enqueue_route(x, W_router, bias, w_shared, c, ids, w, s_shared, st);
   if (s != MOE_OK || gemv_pairs(*c)) return s;
   return enqueue_bucket(ids, c, at<int32_t>(c, p.counts), at<int32_t>(c, p.offsets),
                         at<int32_t>(c, p.active), &at<Ctrl>(c, 0)->n_active,
@@ -601,12 +567,6 @@ size_t moe_workspace_bytes(const moe_cfg_t* cfg) {
   return make_plan(*cfg).total;
 }
 
-size_t moe_layer_l2_prefetch_bytes(const moe_cfg_t* cfg) {
-  if (validate_cfg(cfg) != MOE_OK) return 0;
-  const moe_bank_t none{};
-  return (size_t)(2 * l2_prefetch_plan(*cfg, none, none).bytes);
-}
-
 moe_status_t moe_workspace_init(const moe_cfg_t* cfg, void* stream) {
   if (!cfg || !cfg->workspace || ((uintptr_t)cfg->workspace & 255u) ||
       cfg->workspace_bytes < sizeof(Ctrl))
@@ -737,7 +697,7 @@ moe_status_t moe_layer_forward(const void* x, const float* r_attn, const void* W
   const Plan p = make_plan(*cfg);
   float* s_sh = shared ? at<float>(cfg, p.s_shared) : nullptr;
   s = enqueue_route_bucket(x, W_router, expert_bias, shared ? w_shared : nullptr, cfg, topk_ids,
-                           weights, s_sh, st, l2_prefetch_plan(*cfg, W_gate, W_up));
+                           weights, s_sh, st);
   if (s != MOE_OK) return s;
   return enqueue_experts(x, r_attn, topk_ids, weights, s_sh, W_gate, W_up, W_down, Ws_gate, Ws_up,
                          Ws_down, cfg, out, st);

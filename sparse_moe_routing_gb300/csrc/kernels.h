@@ -16,11 +16,6 @@ struct RouterArgs {
   const void* w_shared;   // [d] or null (then no column E)
   float* logits;          // [T][E+1] f32
   int T, d, E;
-  // optional L2 prefetch issued alongside the logits: [pf0, pf0 + pf_bytes)
-  // and [pf1, pf1 + pf_bytes), both 16-byte aligned, pf_bytes % 16 == 0
-  const void* pf0;
-  const void* pf1;
-  unsigned long long pf_bytes;
 };
 
 struct TopkArgs {

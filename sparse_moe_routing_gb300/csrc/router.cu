@@ -5,25 +5,6 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// L2 prefetch: bulk prefetches of 16 KB pieces over the two ranges, one piece
-// per thread per pass. Nothing waits on them, and the ranges are weights no
-// kernel of the layer writes, so they may start before the grid dependency.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void l2_prefetch_ranges(const RouterArgs& a) {
-  constexpr unsigned long long kPiece = 16384;
-  const unsigned long long n = (a.pf_bytes + kPiece - 1) / kPiece;  // pieces per range
-  const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
-  for (unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n;
-       i += stride) {
-    const bool first = i < n;
-    const unsigned long long off = (first ? i : i - n) * kPiece;
-    const char* p = static_cast<const char*>(first ? a.pf0 : a.pf1) + off;
-    const unsigned bytes = (unsigned)min(kPiece, a.pf_bytes - off);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-  }
-}
-
-// ---------------------------------------------------------------------------
 // logits: one warp per router row (row E = w_shared), up to 8 tokens per CTA.
 // The CTA first copies its tokens' activation rows into shared memory (all
 // loads in flight at once), so each warp's dot products wait on one round of
@@ -34,10 +15,6 @@ __global__ void __launch_bounds__(128) router_logits_kernel(RouterArgs a, int to
   constexpr int kTok = 8;
   constexpr int kVec = Chunk<TA>::kVec;
   extern __shared__ uint4 xs[];  // [nt][d / kVec] when STAGE
-  if (a.pf_bytes && blockIdx.y == gridDim.y - 1) {  // the extra row of prefetching CTAs
-    l2_prefetch_ranges(a);
-    return;
-  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows = a.E + (a.w_shared ? 1 : 0);
   const int r = blockIdx.x * 4 + warp;
@@ -122,8 +99,7 @@ cudaError_t launch_router_logits(const RouterArgs& ra, bool bf16, cudaStream_t s
   tpc = tpc < 1 ? 1 : (tpc > 8 ? 8 : tpc);
   const bool stage = row_bytes <= 48 * 1024;
   const size_t smem = stage ? (size_t)tpc * row_bytes : 0;
-  // one more row of CTAs issues the L2 prefetch, if any
-  dim3 g1((rows + 3) / 4, (ra.T + tpc - 1) / tpc + (ra.pf_bytes ? 1 : 0));
+  dim3 g1((rows + 3) / 4, (ra.T + tpc - 1) / tpc);
   if (bf16)
     return stage ? launch_pdl(router_logits_kernel<__nv_bfloat16, true>, g1, 128, smem, st, ra, tpc)
                  : launch_pdl(router_logits_kernel<__nv_bfloat16, false>, g1, 128, 0, st, ra, tpc);

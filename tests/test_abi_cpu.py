@@ -51,22 +51,6 @@ def _cfg(**kw):
     return smr.MoEConfig(**base)
 
 
-def test_l2_prefetch_budget(L):
-    # 32 MB over gate + up: 8 experts of 2 x 2 MB at the Qwen3.6 shape, T=64
-    assert smr.layer_l2_prefetch_bytes(_cfg(T=64)) == 8 * 2 * 512 * 2048 * 2  # T k = 2E
-    assert smr.layer_l2_prefetch_bytes(_cfg(T=100)) == 8 * 2 * 512 * 2048 * 2
-    assert smr.layer_l2_prefetch_bytes(_cfg(T=63)) == 0    # many experts idle
-    assert smr.layer_l2_prefetch_bytes(_cfg(T=128)) == 0   # tensor-core router
-    assert smr.layer_l2_prefetch_bytes(_cfg(T=4096)) == 0  # groups span row blocks
-    assert smr.layer_l2_prefetch_bytes(_cfg(T=64, path=smr.PATH_GEMV)) == 0
-    assert smr.layer_l2_prefetch_bytes(_cfg(T=64, expert_dtype=smr.Q4_AFFINE_G64,
-                                            d_ff_shared=0)) == 0
-    # small experts: the budget caps at every expert
-    small = _cfg(T=64, d_model=256, n_experts=16, top_k=2, d_ff=128, d_ff_shared=0)
-    assert smr.layer_l2_prefetch_bytes(small) == 16 * 2 * 128 * 256 * 2
-    assert smr.layer_l2_prefetch_bytes(_cfg(T=64, top_k=0)) == 0  # invalid
-
-
 def test_workspace_bytes_grows_with_T(L):
     a = smr.workspace_bytes(_cfg(T=1))
     b = smr.workspace_bytes(_cfg(T=64))
