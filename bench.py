@@ -21,7 +21,7 @@ the event nodes do not add to the timed step.
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--tokens T]
                        [--workload decode|prefill|deepseek|mixtral]
                        [--path auto|gemv|tc] [--impl ours|reference]
-                       [--no-sweep] [--no-cpu-baseline] [--breakdown]
+                       [--no-sweep] [--no-cpu-baseline] [--no-hot-l2] [--breakdown]
 For N > 1 launch with torchrun (one rank per GPU, NCCL): every rank runs an
 independent replica on its own token batch (the layer has no cross-token
 exchange), so the job processes N*T tokens per step ("scaling": "weak").
@@ -65,6 +65,21 @@ def _peaks():
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
         return 6800.0, 1900.0, "fallback"
+
+
+def _sustained_tflops():
+    """bf16 dense rate measured as a seconds-long loop (the burst figure
+    when only that one is known)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p.get("bf16_tflops_sustained", p["bf16_tflops"]))
+    except Exception:
+        return 1700.0
+
+
+NOMINAL_HBM_GBS = 8000.0  # nominal HBM3e bandwidth of the part, for context
+N_EXTRA_REPLAYS = 9       # timed replays after the first, for the median per step
 
 
 # ----------------------------------------------------------------------------
@@ -272,8 +287,10 @@ def _n_copies(shape, T):
     return int(min(16, max(2, math.ceil(4 * L2_BYTES / touched) + 1)))
 
 
-def time_graph(wl, K, W, trace_kernel=None, sampler=None):
-    """Eager warm-up, then one CUDA graph of K steps replayed once (timed)."""
+def time_graph(wl, K, W, trace_kernel=None, sampler=None, extra_replays=0):
+    """Eager warm-up, then one CUDA graph of K steps replayed once (timed);
+    extra_replays more timed replays after it (their ms in the last slot of
+    the result)."""
     import torch
     import sparse_moe_routing_gb300 as smr
     for i in range(W):
@@ -316,8 +333,15 @@ def time_graph(wl, K, W, trace_kernel=None, sampler=None):
         sampler.stop()
     ms = s.elapsed_time(e)
     durs = tr.durations_ms() if tr else []
+    extra = []
+    for _ in range(extra_replays):
+        s.record()
+        g.replay()
+        e.record()
+        torch.cuda.synchronize()
+        extra.append(s.elapsed_time(e))
     del g
-    return ms, launches, durs, (t0, t1)
+    return ms, launches, durs, (t0, t1), extra
 
 
 def time_e2e(wl, K):
@@ -457,6 +481,16 @@ def run_ours(args):
 
     load = {}
 
+    replay_ms = []
+
+    def hot_l2(T):
+        """K steps that reuse one weight copy (no rotation): the weights are
+        L2-resident only where the layer's bytes fit in L2."""
+        wl1 = Workload(weights, T, 1, path)
+        ms1 = time_graph(wl1, K, W)[0]
+        del wl1
+        return ms1 / K
+
     def measure(T, main):
         """The timed replay (no event nodes inside the graph); for the main
         workload also the clocks during it and, from one more replay with
@@ -466,7 +500,10 @@ def run_ours(args):
         tc = _uses_tc(shape, T, path)
         kern = ("tc_gateup" if tc else "gemv_gateup") if main else None
         sampler = ClockSampler(local) if main else None
-        ms, launches, _, (t0, t1) = time_graph(wl, K, W, None, sampler)
+        ms, launches, _, (t0, t1), extra = time_graph(wl, K, W, None, sampler,
+                                                     N_EXTRA_REPLAYS if main else 0)
+        if main:
+            replay_ms[:] = [ms] + extra
         durs = time_graph(wl, min(K, 100), 3, kern)[2] if main else []
         ids = wl.ids.cpu().numpy().ravel()
         n_act = int(np.unique(ids).size)
@@ -520,6 +557,25 @@ def run_ours(args):
               "active_experts": n_act, **load, "layer_alg_bytes": lb, "layer_alg_flops": lf,
               "layer_hbm_frac": lb / (ms_step * 1e-3) / 1e9 / hbm,
               "layer_tensor_frac": lf / (ms_step * 1e-3) / 1e12 / tflops})
+    # the layer's floor: the larger of its bytes at the measured copy rate
+    # and its flops at the measured bf16 rate; fractions also against the
+    # nominal HBM rate and the sustained bf16 rate
+    floor_us = max(lb / (hbm * 1e9), lf / (tflops * 1e12)) * 1e6
+    config.update({
+        "layer_floor_us": floor_us,
+        "layer_floor_frac": floor_us / (ms_step * 1e3),
+        "layer_hbm_frac_nominal_8tbs": lb / (ms_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
+        "layer_tensor_frac_sustained": lf / (ms_step * 1e-3) / 1e12 / _sustained_tflops(),
+        "replays": {"n": len(replay_ms), "steps_each": K,
+                    "ms_per_step_median": float(np.median(replay_ms)) / K,
+                    "ms_per_step_min": min(replay_ms) / K,
+                    "ms_per_step_max": max(replay_ms) / K},
+    })
+    if not args.no_hot_l2:
+        hot = hot_l2(T)
+        config["hot_l2"] = {"ms_per_step": hot, "tokens_per_s": T / (hot * 1e-3),
+                            "note": "one weight copy reused every step (L2-hot where the "
+                                    "layer's bytes fit in L2), not the headline"}
     if not args.no_sweep and args.workload == "decode":
         sweep = {}
         for Ts in (1, 8, 64):
@@ -533,6 +589,8 @@ def run_ours(args):
                               "active_experts": na,
                               "layer_hbm_frac": b / (mss / K * 1e-3) / 1e9 / hbm}
             del wls
+            if not args.no_hot_l2:
+                sweep[str(Ts)]["hot_l2_ms_per_step"] = hot_l2(Ts)
         config["sweep"] = sweep
     if args.breakdown:
         # one more graph replay per kernel family, that family bracketed by
@@ -637,6 +695,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-hot-l2", action="store_true",
+                    help="skip the extra timing with one reused weight copy")
     ap.add_argument("--breakdown", action="store_true",
                     help="also report the mean in-graph time of every kernel family")
     ap.add_argument("--eager", type=int, default=0, metavar="N",
