@@ -34,7 +34,6 @@ namespace {
 constexpr int BM = 128, BK = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStageA = BM * BK * 2;      // 16 KB
-constexpr int kStageB = 256 * BK * 2;     // 32 KB (largest B tile)
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -224,9 +223,14 @@ constexpr int kDequantWarps = 8;
 // per stage, two MMAs per k-block into two 256-column accumulators that fill
 // TMEM), halving the B traffic and the dequantisation per flop; the
 // accumulator is then single-buffered.
-template <bool Q4, int RB, bool EPI>
+// NB = rows of the largest B tile the plan holds: 256, or 128 for bf16
+// gate/up items with 64 + 64-column N tiles (decode batches), whose 32 KB
+// stages leave room for six in flight instead of four.
+template <bool Q4, int RB, bool EPI, int NB = 256>
 struct SmemPlan {
-  static constexpr int kStages = RB == 2 ? (EPI ? 3 : 4) : (Q4 ? 5 : 4);
+  static_assert(NB == 256 || (NB == 128 && !Q4 && RB == 1), "128-row B plan: bf16, unpaired");
+  static constexpr int kStageB = NB * BK * 2;  // bytes of one B stage
+  static constexpr int kStages = NB == 128 ? 6 : (RB == 2 ? (EPI ? 3 : 4) : (Q4 ? 5 : 4));
   static constexpr int kBStages = Q4 ? 2 : kStages;
   static constexpr int kNAcc = 2 / RB;   // accumulator buffers of RB x 256 TMEM columns
   static constexpr int kStageQ = 256 * (BK / 2);  // raw 4-bit codes of one B stage
@@ -236,7 +240,11 @@ struct SmemPlan {
   static constexpr size_t kQ = kB + (size_t)kBStages * kStageB;
   static constexpr size_t kEpi = kQ + (Q4 ? (size_t)kStages * kStageQ : 0);
   static constexpr size_t kBars = kEpi + (EPI ? 4 * (size_t)kEpiWarpBytes : 0);
-  static constexpr size_t kBytes = 1024 + kBars + 256;
+  // full, empty, rawfull per stage; bfull, bempty per B stage; tfull and
+  // tempty per accumulator (two slots each); then the TMEM address word and
+  // the abort flag
+  static constexpr size_t kBarBytes = ((3 * kStages + 2 * kBStages + 4) * 8 + 8 + 127) / 128 * 128;
+  static constexpr size_t kBytes = 1024 + kBars + kBarBytes;
   static_assert(kBytes <= 227 * 1024, "shared memory plan exceeds 227 KB");
 };
 
@@ -306,14 +314,15 @@ __device__ __forceinline__ void dequant_row(const uint8_t* q_row_src, uint8_t* b
   }
 }
 
-template <int MODE, bool Q4, int RB>
-__global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown>::kThreadsCta, 1)
+template <int MODE, bool Q4, int RB, int NB>
+__global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB>::kThreadsCta, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmB3,
                    const TcArgs a) {
-  using SP = SmemPlan<Q4, RB, MODE == kTcDown>;
+  using SP = SmemPlan<Q4, RB, MODE == kTcDown, NB>;
   constexpr int STAGES = SP::kStages;
+  constexpr int kStageB = SP::kStageB;
   constexpr int NACC = SP::kNAcc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -724,16 +733,16 @@ int tc_sm_count() {
 
 namespace {
 
-template <int MODE, bool Q4, int RB>
+template <int MODE, bool Q4, int RB, int NB = 256>
 cudaError_t launch_tc(const TcMaps& maps, const TcArgs& a, int max_items, cudaStream_t st) {
-  using SP = SmemPlan<Q4, RB, MODE == kTcDown>;
+  using SP = SmemPlan<Q4, RB, MODE == kTcDown, NB>;
   static int attr[64] = {};
-  cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE, Q4, RB>, (int)SP::kBytes, attr);
+  cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE, Q4, RB, NB>, (int)SP::kBytes, attr);
   if (e != cudaSuccess) return e;
   int grid = tc_sm_count();
   if (max_items < grid) grid = max_items;
   if (grid < 1) grid = 1;
-  return launch_pdl(tc_gemm_kernel<MODE, Q4, RB>, dim3(grid), SP::kThreadsCta, SP::kBytes, st,
+  return launch_pdl(tc_gemm_kernel<MODE, Q4, RB, NB>, dim3(grid), SP::kThreadsCta, SP::kBytes, st,
                     maps.A0, maps.A1, maps.B0, maps.B1, maps.B2, maps.B3, a);
 }
 
@@ -777,6 +786,7 @@ cudaError_t launch_tc_gemm(int mode, const TcMaps& maps, const TcArgs& a, int ma
               : launch_tc<kTcDown, true, 1>(maps, a, max_items, st);
   }
   if (a.pair) return cudaErrorInvalidValue;  // paired items are built for 4-bit banks only
+  if (up && a.bn <= 128) return launch_tc<kTcGateUp, false, 1, 128>(maps, a, max_items, st);
   return up ? launch_tc<kTcGateUp, false, 1>(maps, a, max_items, st)
             : launch_tc<kTcDown, false, 1>(maps, a, max_items, st);
 }
