@@ -16,8 +16,8 @@
 
 namespace moe {
 
-// Row-block ranking sorts one 64-bit key per group (E + 1 groups, E <= 512)
-// in a power-of-two buffer of at most this many entries.
+// Row-block ranking holds one 64-bit key per group (E + 1 groups, E <= 512)
+// in a buffer of this many entries.
 constexpr int kRankKeys = 1024;
 
 // Shared-memory words bucket_body<NW> needs for E experts: the per-warp
@@ -78,8 +78,8 @@ __device__ __forceinline__ void publish_counts(const BucketArgs& a, const int* c
 // (largest first, ties by lower id; the shared expert is group E with
 // shared_rows rows), then the blocks of bm rows of each (every second block
 // when a.pair: each entry then stands for blocks m and m + 1). The order comes
-// from a bitonic sort of (rows descending, id ascending) keys in `keys`
-// (kRankKeys 8-byte entries); order, nblk: [E+1], bofs: [E+2] scratch. All
+// from ranking (rows descending, id ascending) keys in `keys` (E + 1 8-byte
+// entries) by counting; order, nblk: [E+1], bofs: [E+2] scratch. All
 // threads of the CTA call it.
 template <int NW>
 __device__ __forceinline__ void publish_rowblocks(const BucketArgs& a, const int* cnt,
@@ -102,37 +102,25 @@ __device__ __forceinline__ void publish_rowblocks(const BucketArgs& a, const int
     return;
   }
   const int G = E + (a.shared_rows > 0 ? 1 : 0);
-  int n = 2;
-  while (n < G) n <<= 1;
-  // key: (0xFFFFFFFF - rows) << 32 | id; empty groups and padding sort last
-  for (int g = tid; g < n; g += kThreads) {
-    const int ng = g < E ? cnt[g] : (g == E ? a.shared_rows : 0);
-    keys[g] = (g < G && ng > 0)
-                  ? ((unsigned long long)(0xFFFFFFFFu - (uint32_t)ng) << 32) | (uint32_t)g
-                  : ~0ull;
+  // key: (0xFFFFFFFF - rows) << 32 | id, distinct for the groups with rows;
+  // empty groups get the largest key and take no rank
+  for (int g = tid; g < G; g += kThreads) {
+    const int ng = g < E ? cnt[g] : a.shared_rows;
+    keys[g] = ng > 0 ? ((unsigned long long)(0xFFFFFFFFu - (uint32_t)ng) << 32) | (uint32_t)g
+                     : ~0ull;
   }
   __syncthreads();
-  for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < n / 2; i += kThreads) {
-        const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const unsigned long long x = keys[lo], y = keys[hi];
-        if ((x > y) == up) {
-          keys[lo] = y;
-          keys[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
-  // groups with rows occupy ranks [0, n_nonempty)
+  // a group's rank = the number of keys below its own: groups with rows
+  // occupy ranks [0, n_nonempty) in ascending key order
   const int n_nonempty = aoff[E] + (a.shared_rows > 0 ? 1 : 0);
-  for (int r = tid; r < n_nonempty; r += kThreads) {
-    const unsigned long long k = keys[r];
-    const int ng = (int)(0xFFFFFFFFu - (uint32_t)(k >> 32));
-    order[r] = (int)(k & 0xFFFFFFFFu);
+  for (int g = tid; g < G; g += kThreads) {
+    const unsigned long long kg = keys[g];
+    if (kg == ~0ull) continue;
+    int r = 0;
+#pragma unroll 8
+    for (int h = 0; h < G; ++h) r += keys[h] < kg ? 1 : 0;
+    const int ng = (int)(0xFFFFFFFFu - (uint32_t)(kg >> 32));
+    order[r] = g;
     const int blocks = (ng + a.bm - 1) / a.bm;
     nblk[r] = a.pair ? (blocks + 1) / 2 : blocks;  // list entries: pairs when paired
   }
