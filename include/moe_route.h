@@ -72,7 +72,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,    /* null pointer, bad shape, misalignment, aliasing */
-  MOE_ERR_UNSUPPORTED = 2,    /* valid but outside this build's limits */
+  MOE_ERR_UNSUPPORTED = 2,    /* valid but outside the library's limits */
   MOE_ERR_WORKSPACE = 3,      /* workspace null, too small or misaligned */
   MOE_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
   MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded on-device wait gave up */

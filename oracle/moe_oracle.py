@@ -201,7 +201,7 @@ def sigmoid_group_topk_route(z: np.ndarray, bias, n_group: int, topk_group: int,
 def route_tokens(z: np.ndarray, shape, bias=None) -> dict:
     """Routes every token of z [T][E] by the shape's rule. Returns ids [T][k]
     int32, weights [T][k] float64, and the per-token ranking scores used to
-    judge near-ties: `score` [T][E] (softmax p, or the selection score with
+    classify near-ties: `score` [T][E] (softmax p, or the selection score with
     bias) and, for the sigmoid family, `group_score` [T][n_group]."""
     T, E = z.shape
     k = shape.top_k

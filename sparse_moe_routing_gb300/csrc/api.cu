@@ -131,7 +131,7 @@ moe_status_t validate_cfg(const moe_cfg_t* c) {
       c->expert_dtype != MOE_Q4_AFFINE_G64)
     return MOE_ERR_INVALID_ARG;
   if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_TC) return MOE_ERR_INVALID_ARG;
-  // limits of this build
+  // limits of the library (kernel templates and shared-memory plans)
   if (c->n_experts > 512 || c->top_k > 32) return MOE_ERR_UNSUPPORTED;
   if (c->expert_dtype == MOE_F32 && c->act_dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
   if (c->expert_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
@@ -530,7 +530,7 @@ const char* moe_status_string(moe_status_t s) {
   switch (s) {
     case MOE_OK: return "MOE_OK";
     case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
-    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: outside this build's limits";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: outside the library's limits";
     case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace null, too small or misaligned";
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or launch failed";
     case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
