@@ -359,7 +359,8 @@ moe_status_t enqueue_route_bucket(const void* x, const void* W_router, const flo
 moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float* alpha,
                                 const float* s_shared, moe_bank_t Wg, moe_bank_t Wu,
                                 moe_bank_t Wd, const void* Wsg, const void* Wsu, const void* Wsd,
-                                const moe_cfg_t* c, float* out, cudaStream_t st) {
+                                const moe_cfg_t* c, float* out, cudaStream_t st,
+                                bool ids_distinct) {
   const Plan p = make_plan(*c);
   Ctrl* ctrl = at<Ctrl>(c, 0);
   const int T = c->T, d = c->d_model, E = c->n_experts, k = c->top_k, I = c->d_ff;
@@ -391,6 +392,11 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
   a.pair = use_pair(*c) ? 1 : 0;
 
   const bool q4 = c->expert_dtype == MOE_Q4_AFFINE_G64;
+  // A tiles only as tall as the tallest group can be: with ids from the
+  // routing rule (k distinct experts per token) every routed group holds at
+  // most T rows, and the shared expert holds T
+  const uint32_t arows = (!q4 && ids_distinct) ? (T <= 16 ? 16u : (T <= 64 ? 64u : 128u)) : 128u;
+  a.arows = (int)arows;
   auto bmap = [&](CUtensorMap* mp, const void* w, uint64_t rows, uint64_t K, uint32_t box) {
     return q4 ? tc_make_map_q4(mp, w, rows, K, box) : tc_make_map(mp, w, rows, K, box);
   };
@@ -402,7 +408,7 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
   const int gu_bn = (!q4 && (long long)max_rb * (I / 128) < 4LL * tc_sm_count()) ? 128 : 256;
   const uint32_t gu_rows = gu_bn / 2;
   TcMaps m{};
-  bool ok = tc_make_map(&m.A0, xperm, P, d, 128) && tc_make_map(&m.A1, x, T, d, 128) &&
+  bool ok = tc_make_map(&m.A0, xperm, P, d, arows) && tc_make_map(&m.A1, x, T, d, arows) &&
             bmap(&m.B0, Wg.w, (uint64_t)E * I, d, gu_rows) &&
             bmap(&m.B1, Wu.w, (uint64_t)E * I, d, gu_rows);
   if (q4) {
@@ -432,14 +438,15 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
 
   // down: A = H (routed) / Hs (shared), B = down rows; alpha in the epilogue
   TcMaps m2{};
-  ok = tc_make_map(&m2.A0, H, P, I, 128) && bmap(&m2.B0, Wd.w, (uint64_t)E * d, I, 256);
+  ok = tc_make_map(&m2.A0, H, P, I, arows) && bmap(&m2.B0, Wd.w, (uint64_t)E * d, I, 256);
   if (q4) {
     a.qs0 = static_cast<const __nv_bfloat16*>(Wd.scale);
     a.qm0 = static_cast<const __nv_bfloat16*>(Wd.minv);
     a.qs1 = a.qm1 = nullptr;
     a.qgroups = I / 64;
   }
-  if (ok && shared) ok = tc_make_map(&m2.A1, Hs, T, Is, 128) && tc_make_map(&m2.B2, Wsd, d, Is, 256);
+  if (ok && shared)
+    ok = tc_make_map(&m2.A1, Hs, T, Is, arows) && tc_make_map(&m2.B2, Wsd, d, Is, 256);
   if (!ok) return MOE_ERR_CUDA;
   if (!shared) {
     m2.A1 = m2.A0;
@@ -467,9 +474,11 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
 moe_status_t enqueue_experts(const void* x, const float* r_attn, const int32_t* ids,
                              const float* alpha, const float* s_shared, moe_bank_t Wg,
                              moe_bank_t Wu, moe_bank_t Wd, const void* Wsg, const void* Wsu,
-                             const void* Wsd, const moe_cfg_t* c, float* out, cudaStream_t st) {
+                             const void* Wsd, const moe_cfg_t* c, float* out, cudaStream_t st,
+                             bool ids_distinct) {
   if (use_tc(*c))
-    return enqueue_experts_tc(x, r_attn, alpha, s_shared, Wg, Wu, Wd, Wsg, Wsu, Wsd, c, out, st);
+    return enqueue_experts_tc(x, r_attn, alpha, s_shared, Wg, Wu, Wd, Wsg, Wsu, Wsd, c, out, st,
+                              ids_distinct);
   const Plan p = make_plan(*c);
   Ctrl* ctrl = at<Ctrl>(c, 0);
   GemvArgs g{};
@@ -667,7 +676,7 @@ moe_status_t moe_experts_forward(const void* x, const float* r_attn, const int32
     if (s != MOE_OK) return s;
   }
   return enqueue_experts(x, r_attn, topk_ids, weights, s_shared, W_gate, W_up, W_down, Ws_gate,
-                         Ws_up, Ws_down, cfg, out, st);
+                         Ws_up, Ws_down, cfg, out, st, /*ids_distinct=*/false);
 }
 
 moe_status_t moe_layer_forward(const void* x, const float* r_attn, const void* W_router,
@@ -700,7 +709,7 @@ moe_status_t moe_layer_forward(const void* x, const float* r_attn, const void* W
                            weights, s_sh, st);
   if (s != MOE_OK) return s;
   return enqueue_experts(x, r_attn, topk_ids, weights, s_sh, W_gate, W_up, W_down, Ws_gate, Ws_up,
-                         Ws_down, cfg, out, st);
+                         Ws_down, cfg, out, st, /*ids_distinct=*/true);
 }
 
 }  // extern "C"

@@ -114,6 +114,9 @@ struct TcArgs {
   // the B tiles (the bucketing pass then lists every second block); 4-bit
   // banks only
   int pair;
+  // box height of the A maps (gate/up and down, bf16): 128, or 64 / 16 when
+  // every group holds at most that many rows
+  int arows;
 };
 
 // The six operand maps: A routed/shared, B0/B1 routed, B2/B3 shared.

@@ -33,7 +33,6 @@ namespace {
 // epilogue, and (4-bit weights only) warps 6-13 dequantise the B stages.
 constexpr int BM = 128, BK = 64;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kStageA = BM * BK * 2;      // 16 KB
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -224,13 +223,25 @@ constexpr int kDequantWarps = 8;
 // TMEM), halving the B traffic and the dequantisation per flop; the
 // accumulator is then single-buffered.
 // NB = rows of the largest B tile the plan holds: 256, or 128 for bf16
-// gate/up items with 64 + 64-column N tiles (decode batches), whose 32 KB
-// stages leave room for six in flight instead of four.
-template <bool Q4, int RB, bool EPI, int NB = 256>
+// gate/up items with 64 + 64-column N tiles (decode batches).
+// AR = rows of the A tile TMA brings per stage: 128, or 64 / 16 for bf16
+// decode batches whose groups all hold at most that many rows. The MMA still
+// reads 128 A rows from the stage's base; rows past AR hold whatever the
+// following shared memory holds and only feed accumulator rows past the
+// group's last row, which the epilogue never stores.
+// The narrower plans (NB < 256 or AR < 128) fit as many stages as 227 KB
+// allows, at most 12, so that more weight bytes are in flight per SM.
+template <bool Q4, int RB, bool EPI, int NB = 256, int AR = 128>
 struct SmemPlan {
   static_assert(NB == 256 || (NB == 128 && !Q4 && RB == 1), "128-row B plan: bf16, unpaired");
+  static_assert(AR == 128 || ((AR == 64 || AR == 16) && !Q4 && RB == 1), "short A: bf16, unpaired");
+  static constexpr int kStageA = AR * BK * 2;  // bytes of one A stage
   static constexpr int kStageB = NB * BK * 2;  // bytes of one B stage
-  static constexpr int kStages = NB == 128 ? 6 : (RB == 2 ? (EPI ? 3 : 4) : (Q4 ? 5 : 4));
+  static constexpr size_t kEpiBytes = EPI ? 4 * (size_t)kEpiWarpBytes : 0;
+  static constexpr int kFit = (int)((227 * 1024 - 2048 - kEpiBytes) / (kStageA + kStageB));
+  static constexpr bool kNarrow = !Q4 && RB == 1 && (NB < 256 || AR < 128);
+  static constexpr int kStages =
+      kNarrow ? (kFit > 12 ? 12 : kFit) : (RB == 2 ? (EPI ? 3 : 4) : (Q4 ? 5 : 4));
   static constexpr int kBStages = Q4 ? 2 : kStages;
   static constexpr int kNAcc = 2 / RB;   // accumulator buffers of RB x 256 TMEM columns
   static constexpr int kStageQ = 256 * (BK / 2);  // raw 4-bit codes of one B stage
@@ -239,7 +250,7 @@ struct SmemPlan {
   static constexpr size_t kB = kA + (size_t)kStages * RB * kStageA;
   static constexpr size_t kQ = kB + (size_t)kBStages * kStageB;
   static constexpr size_t kEpi = kQ + (Q4 ? (size_t)kStages * kStageQ : 0);
-  static constexpr size_t kBars = kEpi + (EPI ? 4 * (size_t)kEpiWarpBytes : 0);
+  static constexpr size_t kBars = kEpi + kEpiBytes;
   // full, empty, rawfull per stage; bfull, bempty per B stage; tfull and
   // tempty per accumulator (two slots each); then the TMEM address word and
   // the abort flag
@@ -314,14 +325,15 @@ __device__ __forceinline__ void dequant_row(const uint8_t* q_row_src, uint8_t* b
   }
 }
 
-template <int MODE, bool Q4, int RB, int NB>
-__global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB>::kThreadsCta, 1)
+template <int MODE, bool Q4, int RB, int NB, int AR>
+__global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kThreadsCta, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmB3,
                    const TcArgs a) {
-  using SP = SmemPlan<Q4, RB, MODE == kTcDown, NB>;
+  using SP = SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>;
   constexpr int STAGES = SP::kStages;
+  constexpr int kStageA = SP::kStageA;
   constexpr int kStageB = SP::kStageB;
   constexpr int NACC = SP::kNAcc;
   extern __shared__ uint8_t smem_raw[];
@@ -733,16 +745,16 @@ int tc_sm_count() {
 
 namespace {
 
-template <int MODE, bool Q4, int RB, int NB = 256>
+template <int MODE, bool Q4, int RB, int NB = 256, int AR = 128>
 cudaError_t launch_tc(const TcMaps& maps, const TcArgs& a, int max_items, cudaStream_t st) {
-  using SP = SmemPlan<Q4, RB, MODE == kTcDown, NB>;
+  using SP = SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>;
   static int attr[64] = {};
-  cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE, Q4, RB, NB>, (int)SP::kBytes, attr);
+  cudaError_t e = ensure_smem_limit(tc_gemm_kernel<MODE, Q4, RB, NB, AR>, (int)SP::kBytes, attr);
   if (e != cudaSuccess) return e;
   int grid = tc_sm_count();
   if (max_items < grid) grid = max_items;
   if (grid < 1) grid = 1;
-  return launch_pdl(tc_gemm_kernel<MODE, Q4, RB, NB>, dim3(grid), SP::kThreadsCta, SP::kBytes, st,
+  return launch_pdl(tc_gemm_kernel<MODE, Q4, RB, NB, AR>, dim3(grid), SP::kThreadsCta, SP::kBytes, st,
                     maps.A0, maps.A1, maps.B0, maps.B1, maps.B2, maps.B3, a);
 }
 
@@ -786,9 +798,21 @@ cudaError_t launch_tc_gemm(int mode, const TcMaps& maps, const TcArgs& a, int ma
               : launch_tc<kTcDown, true, 1>(maps, a, max_items, st);
   }
   if (a.pair) return cudaErrorInvalidValue;  // paired items are built for 4-bit banks only
-  if (up && a.bn <= 128) return launch_tc<kTcGateUp, false, 1, 128>(maps, a, max_items, st);
-  return up ? launch_tc<kTcGateUp, false, 1>(maps, a, max_items, st)
-            : launch_tc<kTcDown, false, 1>(maps, a, max_items, st);
+  // the A maps' box height is a.arows: 128, or 64 / 16 for decode batches
+  if (a.arows != 128 && a.arows != 64 && a.arows != 16) return cudaErrorInvalidValue;
+  if (up && a.bn <= 128) {
+    if (a.arows == 16) return launch_tc<kTcGateUp, false, 1, 128, 16>(maps, a, max_items, st);
+    if (a.arows == 64) return launch_tc<kTcGateUp, false, 1, 128, 64>(maps, a, max_items, st);
+    return launch_tc<kTcGateUp, false, 1, 128>(maps, a, max_items, st);
+  }
+  if (up) {
+    if (a.arows == 16) return launch_tc<kTcGateUp, false, 1, 256, 16>(maps, a, max_items, st);
+    if (a.arows == 64) return launch_tc<kTcGateUp, false, 1, 256, 64>(maps, a, max_items, st);
+    return launch_tc<kTcGateUp, false, 1>(maps, a, max_items, st);
+  }
+  if (a.arows == 16) return launch_tc<kTcDown, false, 1, 256, 16>(maps, a, max_items, st);
+  if (a.arows == 64) return launch_tc<kTcDown, false, 1, 256, 64>(maps, a, max_items, st);
+  return launch_tc<kTcDown, false, 1>(maps, a, max_items, st);
 }
 
 }  // namespace moe
