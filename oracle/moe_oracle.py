@@ -46,7 +46,7 @@ __all__ = [
     "bf16_bits_to_f64", "to_f64", "dequant_q4_affine_g64", "ExpertBanks",
     "router_logits", "softmax", "topk_desc", "renormalise_clamped",
     "softmax_topk_route", "sigmoid", "sigmoid_group_topk_route",
-    "route_tokens", "silu", "swiglu_expert", "shared_gate",
+    "route_tokens", "selection_weights", "silu", "swiglu_expert", "shared_gate",
     "moe_layer_forward", "moe_experts_forward", "bucket",
 ]
 
@@ -198,11 +198,31 @@ def sigmoid_group_topk_route(z: np.ndarray, bias, n_group: int, topk_group: int,
     return ids, weights, sel, group_scores, kept
 
 
+def selection_weights(z: np.ndarray, ids, shape, bias=None) -> np.ndarray:
+    """The weight step of the shape's rule applied to a given selection `ids`
+    of one token with logits z [E] (the last step of [P1] "Routing math" /
+    [P2] "Softmax top-k": the selected probabilities renormalised with the
+    clamp; of [P2] "Sigmoid group top-k": the selected raw sigmoid scores,
+    no bias, normalised to one), times routed_scaling. For the oracle's own
+    selection this is the weight route_tokens returns; for another valid
+    selection of a near-tied token it is the weight that selection carries.
+    `bias` is accepted for symmetry with the rules and never enters."""
+    ids = np.asarray(ids, dtype=np.int64)
+    if shape.router == "softmax":
+        p = softmax(z)
+        return renormalise_clamped(p[ids], shape.renorm_clamp) * shape.routed_scaling
+    if shape.router == "sigmoid_group":
+        raw = sigmoid(np.asarray(z, dtype=np.float64)[ids])
+        return raw / np.sum(raw) * shape.routed_scaling
+    raise ValueError(shape.router)
+
+
 def route_tokens(z: np.ndarray, shape, bias=None) -> dict:
     """Routes every token of z [T][E] by the shape's rule. Returns ids [T][k]
     int32, weights [T][k] float64, and the per-token ranking scores used to
     classify near-ties: `score` [T][E] (softmax p, or the selection score with
-    bias) and, for the sigmoid family, `group_score` [T][n_group]."""
+    bias) and, for the sigmoid family, `group_score` [T][n_group]; `logits`
+    and `bias` are the inputs, returned for selection_weights."""
     T, E = z.shape
     k = shape.top_k
     ids = np.zeros((T, k), dtype=np.int32)
@@ -224,7 +244,8 @@ def route_tokens(z: np.ndarray, shape, bias=None) -> dict:
             raise ValueError(shape.router)
         ids[t] = i
         w[t] = a
-    return {"ids": ids, "weights": w, "score": score, "group_score": gsc}
+    return {"ids": ids, "weights": w, "score": score, "group_score": gsc, "logits": z,
+            "bias": bias}
 
 
 # ----------------------------------------------------------------------------

@@ -7,16 +7,24 @@ Criteria (stated once here, applied throughout):
   * routing weights: within 1e-5 absolute;
   * bucketing: bit-exact (integers);
   * layer output: max |out - ref| / rms(ref) <= 2e-2 (bf16) or 1e-4 (fp32).
+  * the layer's own contribution y_moe = out - r_attn: the same metric
+    <= 3e-2 (bf16) or 1e-3 (fp32);
+  * near-tie tokens: the GPU's selection must be one the criteria accept,
+    with the weights the oracle's rule gives it, and its output row is
+    compared with the oracle's output for that selection.
 Small cases compare every element; full-size cases compare the routing of
-every token and the outputs of a seeded sample of tokens (each output row
-depends only on its own token, so the oracle computes sampled rows exactly).
+every token and the output rows that cover every work item of the grouped
+GEMMs (the first and last packed row of every 128-row block of every expert
+and of the shared expert), plus a seeded sample (each output row depends
+only on its own token, so the oracle computes those rows exactly).
 """
 import numpy as np
 import pytest
 
 import moe_inputs as mi
 import oracle as orc
-from gpu_util import (OUT_TOL, DevLayer, cfg_for, check_routing, layer_host, rel_rms_err,
+from gpu_util import (OUT_TOL, Y_TOL, DevLayer, block_rows, cfg_for, check_layer,
+                      check_routing, layer_host, oracle_banks, oracle_routing, rel_rms_err,
                       to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -33,13 +41,6 @@ def _built():
     from sparse_moe_routing_gb300 import build
     build.build()
     smr.lib()
-
-
-def _oracle_routing(L, shape):
-    x = orc.to_f64(L["x"], shape.act_dtype)
-    W = orc.to_f64(L["W_router"], shape.act_dtype)
-    bias = None if "expert_bias" not in L else L["expert_bias"].astype(np.float64)
-    return orc.route_tokens(orc.router_logits(x, W), shape, bias)
 
 
 def _sample(T, n, seed=0):
@@ -61,53 +62,59 @@ def _run_layer(shape, T, path=smr.PATH_AUTO):
     return L, dev, cfg, ws
 
 
-# (shape, T, number of output rows the oracle checks)
+# (shape, T, output rows the oracle checks: "all", or "blocks" for the rows
+# covering every 128-row block of every group plus a seeded sample)
 CASES = [
-    (mi.TINY_F32, 32, 32),
-    (mi.TINY_F32.with_(name="tiny_f32_ragged"), 37, 37),
-    (mi.TINY_F32.with_(name="tiny_f32_t4"), 4, 4),
-    (mi.QWEN36, 1, 1),
-    (mi.QWEN36, 2, 2),
-    (mi.QWEN36, 3, 3),
-    (mi.QWEN36, 8, 8),
-    (mi.QWEN36, 64, 64),
-    (mi.QWEN36, 37, 37),
-    (mi.DEEPSEEK_GROUP, 1, 1),
-    (mi.DEEPSEEK_GROUP, 64, 64),
-    (mi.QWEN36_PREFILL_SKEW, 4096, 24),
-    (mi.DEEPSEEK_GROUP, 4096, 24),
-    (mi.MIXTRAL, 2048, 6),
-    (mi.DEEPSEEK_MOE_64, 1, 1),
-    (mi.DEEPSEEK_MOE_64, 256, 12),
-    (mi.QWEN_MOE_60, 1, 1),
-    (mi.QWEN_MOE_60, 5, 5),
-    (mi.DEEPSEEK_V2_160, 64, 12),
-    (mi.DEEPSEEK_V2_160, 1024, 12),
+    (mi.TINY_F32, 32, "all"),
+    (mi.TINY_F32.with_(name="tiny_f32_ragged"), 37, "all"),
+    (mi.TINY_F32.with_(name="tiny_f32_t4"), 4, "all"),
+    (mi.QWEN36, 1, "all"),
+    (mi.QWEN36, 2, "all"),
+    (mi.QWEN36, 3, "all"),
+    (mi.QWEN36, 8, "all"),
+    (mi.QWEN36, 16, "all"),
+    (mi.QWEN36, 17, "all"),
+    (mi.QWEN36, 64, "all"),
+    (mi.QWEN36, 65, "all"),
+    (mi.QWEN36, 37, "all"),
+    (mi.DEEPSEEK_GROUP, 1, "all"),
+    (mi.DEEPSEEK_GROUP, 64, "all"),
+    (mi.QWEN36_PREFILL_SKEW, 4096, "blocks"),
+    (mi.DEEPSEEK_GROUP, 4096, "blocks"),
+    (mi.MIXTRAL, 2048, "blocks"),
+    (mi.DEEPSEEK_MOE_64, 1, "all"),
+    (mi.DEEPSEEK_MOE_64, 256, "blocks"),
+    (mi.QWEN_MOE_60, 1, "all"),
+    (mi.QWEN_MOE_60, 5, "all"),
+    (mi.DEEPSEEK_V2_160, 64, "all"),
+    (mi.DEEPSEEK_V2_160, 1024, "blocks"),
 ]
 
 
-@pytest.mark.parametrize("shape,T,n_check", CASES,
+def _check_rows(L, shape, T, dev, mode, seed=0):
+    """Routing of every token and the chosen output rows against the oracle;
+    prints and returns (near-ties, rerouted tokens, out error, y_moe error)."""
+    ref_r = oracle_routing(L, shape)
+    if mode == "all":
+        rows, blocks = np.arange(T), None
+    else:
+        rows, blocks = block_rows(ref_r, shape, T, extra=_sample(T, 16, seed))
+    res = check_layer(L, shape, dev.ids.cpu().numpy(), dev.w.cpu().numpy(),
+                      dev.out.cpu().numpy(), rows, ref_r, oracle_banks(L, shape))
+    near, moved, err, y_err = res
+    print("%s T=%d rows=%d%s near-ties=%d rerouted=%d out_err=%.3e y_moe_err=%.3e" % (
+        shape.name, T, len(rows), "" if blocks is None else " blocks=%d/%d" % (blocks, blocks),
+        near, moved, err, y_err))
+    assert err <= OUT_TOL[shape.act_dtype], err
+    assert y_err <= Y_TOL[shape.act_dtype], y_err
+    return res
+
+
+@pytest.mark.parametrize("shape,T,mode", CASES,
                          ids=["%s-T%d" % (c[0].name, c[1]) for c in CASES])
-def test_layer_forward_parity(shape, T, n_check):
+def test_layer_forward_parity(shape, T, mode):
     L, dev, cfg, ws = _run_layer(shape, T)
-    gpu_ids = dev.ids.cpu().numpy()
-    gpu_w = dev.w.cpu().numpy()
-    out = dev.out.cpu().numpy()
-    # routing of every token
-    ref_r = _oracle_routing(L, shape)
-    near = check_routing(gpu_ids, gpu_w, ref_r, shape)
-    # output rows of a sample whose GPU ids equal the oracle's
-    rows = _sample(T, n_check)
-    ref = orc.moe_layer_forward(L, shape, tokens=rows)
-    agree = [i for i, t in enumerate(rows) if sorted(gpu_ids[t]) == sorted(ref["ids"][i])]
-    assert len(agree) >= len(rows) - max(1, near)
-    tol = OUT_TOL[shape.act_dtype]
-    err = rel_rms_err(out[rows[agree]], ref["out"][agree])
-    y_err = rel_rms_err(out[rows[agree]] - L["r_attn"][rows[agree]],
-                        ref["out"][agree] - L["r_attn"][rows[agree]])
-    print("%s T=%d near-ties=%d out_err=%.3e y_moe_err=%.3e" % (shape.name, T, near, err, y_err))
-    assert err <= tol, err
-    assert y_err <= 10 * tol, y_err
+    _check_rows(L, shape, T, dev, mode)
 
 
 ROUTE_CASES = [(mi.TINY_F32, 32), (mi.QWEN36, 64), (mi.QWEN36_PREFILL_SKEW, 4096),
@@ -126,7 +133,7 @@ def test_route_parity_and_shared_gate(shape, T):
               expert_bias=dev.t.get("expert_bias"), w_shared=dev.t.get("w_shared"),
               s_shared=s_sh)
     assert smr.read_device_status(cfg, ws)[0] == 0
-    ref = _oracle_routing(L, shape)
+    ref = oracle_routing(L, shape)
     check_routing(dev.ids.cpu().numpy(), dev.w.cpu().numpy(), ref, shape)
     if s_sh is not None:
         x = orc.to_f64(L["x"], shape.act_dtype)
@@ -372,7 +379,11 @@ def test_zero_tokens_is_a_no_op():
 # (I = 256) and two of down (d = 512), with a full fp64 oracle.
 TC_SMALL = mi.MoEShape("tc_small", 7, d_model=512, n_experts=4, top_k=2, d_ff=256,
                        d_ff_shared=256, tokens=(400,))
+# Qwen3.6 at T = 16, 17, 64, 65: the A tiles of routed batches are 16 rows
+# tall up to T = 16 and 64 rows up to T = 64 (the shared expert's group holds
+# all T rows), so these sit at and just past each box edge.
 PATH_CASES = [(TC_SMALL, 400), (TC_SMALL, 700), (TC_SMALL, 37), (TC_SMALL, 1), (mi.QWEN36, 64),
+              (mi.QWEN36, 16), (mi.QWEN36, 17), (mi.QWEN36, 65),
               (mi.QWEN36, 8), (mi.QWEN36, 5), (mi.DEEPSEEK_GROUP, 6),
               (mi.DEEPSEEK_GROUP, 37)]
 
@@ -384,17 +395,7 @@ def test_both_expert_paths_match_oracle(shape, T, path):
     """The CUDA-core streaming path and the tcgen05 grouped-GEMM path, each
     forced, against the oracle on every output row."""
     L, dev, cfg, ws = _run_layer(shape, T, path)
-    ref = orc.moe_layer_forward(L, shape)
-    ids = dev.ids.cpu().numpy()
-    near = check_routing(ids, dev.w.cpu().numpy(), ref, shape)
-    agree = [t for t in range(T) if sorted(ids[t]) == sorted(ref["ids"][t])]
-    assert len(agree) >= T - max(1, near)
-    out = dev.out.cpu().numpy()
-    err = rel_rms_err(out[agree], ref["out"][agree])
-    y_err = rel_rms_err(out[agree] - L["r_attn"][agree], ref["out"][agree] - L["r_attn"][agree])
-    print("%s T=%d path=%d out_err=%.3e y_moe_err=%.3e" % (shape.name, T, path, err, y_err))
-    assert err <= OUT_TOL[shape.act_dtype]
-    assert y_err <= 10 * OUT_TOL[shape.act_dtype]
+    _check_rows(L, shape, T, dev, "all")
 
 
 # 4-bit affine group-64 experts (dequantised inside the tensor-core kernel):
@@ -403,28 +404,15 @@ Q4_SMALL = mi.MoEShape("q4_small", 8, d_model=512, n_experts=4, top_k=2, d_ff=25
                        d_ff_shared=0, expert_dtype="q4", tokens=(300,))
 # T=700: 350 rows per expert on average, so the 4-bit items pair row blocks
 # (with ragged pairs at every group's end)
-Q4_CASES = [(Q4_SMALL, 300, 300), (Q4_SMALL, 700, 40), (Q4_SMALL, 37, 37), (Q4_SMALL, 1, 1),
-            (mi.MIXTRAL_Q4, 2048, 6)]
+Q4_CASES = [(Q4_SMALL, 300, "all"), (Q4_SMALL, 700, "all"), (Q4_SMALL, 37, "all"),
+            (Q4_SMALL, 1, "all"), (mi.MIXTRAL_Q4, 2048, "blocks")]
 
 
-@pytest.mark.parametrize("shape,T,n_check", Q4_CASES,
+@pytest.mark.parametrize("shape,T,mode", Q4_CASES,
                          ids=["%s-T%d" % (c[0].name, c[1]) for c in Q4_CASES])
-def test_q4_layer_forward_parity(shape, T, n_check):
+def test_q4_layer_forward_parity(shape, T, mode):
     L, dev, cfg, ws = _run_layer(shape, T)
-    ids = dev.ids.cpu().numpy()
-    ref_r = _oracle_routing(L, shape)
-    near = check_routing(ids, dev.w.cpu().numpy(), ref_r, shape)
-    rows = _sample(T, n_check, seed=5)
-    ref = orc.moe_layer_forward(L, shape, tokens=rows)
-    agree = [i for i, t in enumerate(rows) if sorted(ids[t]) == sorted(ref["ids"][i])]
-    assert len(agree) >= len(rows) - max(1, near)
-    out = dev.out.cpu().numpy()
-    err = rel_rms_err(out[rows[agree]], ref["out"][agree])
-    y_err = rel_rms_err(out[rows[agree]] - L["r_attn"][rows[agree]],
-                        ref["out"][agree] - L["r_attn"][rows[agree]])
-    print("%s T=%d out_err=%.3e y_moe_err=%.3e" % (shape.name, T, err, y_err))
-    assert err <= OUT_TOL["bf16"], err
-    assert y_err <= 10 * OUT_TOL["bf16"], y_err
+    _check_rows(L, shape, T, dev, mode, seed=5)
 
 
 def test_q4_experts_forward_given_routing():
