@@ -211,14 +211,23 @@ MOE_API moe_status_t moe_route(const void* x, const void* W_router,
  * memory (a plugin whose host framework owns every allocation and offers no
  * allocator; a serving loop that must not allocate once running, because an
  * allocation can synchronise the device). The pages have no counterpart:
- * this is a packaging of moe_route, with the same arguments, results and
- * errors, except that the router logits live in a fixed array inside the
- * library (4 MiB, held on every device that loads the library until exit)
- * instead of cfg->workspace, which is ignored. Allocates nothing.
- * - T * (E + 1) must not exceed 1,048,576 (MOE_ERR_UNSUPPORTED otherwise).
+ * this is a packaging of moe_route, with the same arguments and outputs,
+ * except that the router logits live in a fixed array inside the library
+ * (4 MiB, held on every device that loads the library until exit) instead
+ * of cfg->workspace, which is ignored. Allocates nothing.
+ * - Routing follows moe_route's CUDA-core router at every T (moe_route
+ *   uses a tensor-core router contraction from 128 bf16 tokens; the two
+ *   logits may differ in their last bits, so near-tied ids may differ).
+ * - Errors: moe_route's argument checks and codes, without the workspace
+ *   check; in addition T * (E + 1) above 1,048,576 returns
+ *   MOE_ERR_UNSUPPORTED. A failed lookup or launch returns MOE_ERR_CUDA
+ *   with its text in moe_last_cuda_error.
  * - The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
- * - All calls share the array: calls whose kernels overlap on the GPU race
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture. A device reset invalidates the lookup: do
+ *   not call this entry point on a device after resetting it.
+ * - All calls share the array, which keeps the last call's logits: calls
+ *   whose kernels overlap on the GPU (two streams, two threads) race on it
  *   and must be serialised by the caller.
  * - Its launches are not counted by moe_launch_count nor traced. */
 MOE_API moe_status_t moe_route_static(const void* x, const void* W_router,

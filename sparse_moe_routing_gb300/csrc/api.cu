@@ -109,6 +109,8 @@ Plan make_plan(const moe_cfg_t& c) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+}  // namespace
+
 moe_status_t validate_cfg(const moe_cfg_t* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->T < 0 || c->d_model <= 0 || (c->d_model % 8) != 0) return MOE_ERR_INVALID_ARG;
@@ -143,6 +145,15 @@ moe_status_t validate_cfg(const moe_cfg_t* c) {
   return MOE_OK;
 }
 
+moe_status_t validate_route_cfg(const moe_cfg_t* c) {
+  moe_status_t s = validate_cfg(c);
+  if (s != MOE_OK && s != MOE_ERR_UNSUPPORTED) return s;
+  if (c->n_experts > 512 || c->top_k > 32 || c->n_group > 32) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+namespace {
+
 moe_status_t check_workspace(const moe_cfg_t* c) {
   if (!c->workspace || ((uintptr_t)c->workspace & 255u)) return MOE_ERR_WORKSPACE;
   if (c->workspace_bytes < make_plan(*c).total) return MOE_ERR_WORKSPACE;
@@ -154,8 +165,14 @@ T* at(const moe_cfg_t* c, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(c->workspace) + off);
 }
 
+}  // namespace
+
 // Last CUDA error seen by a call of this thread (moe_last_cuda_error).
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+void set_last_cuda_error(cudaError_t e) { g_last_cuda_error = e; }
+
+namespace {
 
 moe_status_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;
@@ -602,9 +619,8 @@ moe_status_t moe_read_device_status(const moe_cfg_t* cfg, void* stream, uint32_t
 moe_status_t moe_route(const void* x, const void* W_router, const float* expert_bias,
                        const void* w_shared, const moe_cfg_t* cfg, int32_t* topk_ids,
                        float* weights, float* s_shared, void* stream) {
-  moe_status_t s = validate_cfg(cfg);
-  if (s != MOE_OK && s != MOE_ERR_UNSUPPORTED) return s;
-  if (cfg->n_experts > 512 || cfg->top_k > 32 || cfg->n_group > 32) return MOE_ERR_UNSUPPORTED;
+  moe_status_t s = validate_route_cfg(cfg);
+  if (s != MOE_OK) return s;
   if ((s = check_workspace(cfg)) != MOE_OK) return s;
   if (cfg->T == 0) return MOE_OK;
   if (!x || !W_router || !topk_ids || !weights) return MOE_ERR_INVALID_ARG;

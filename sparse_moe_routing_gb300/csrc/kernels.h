@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "moe_route.h"
+
 namespace moe {
 
 struct Ctrl;
@@ -171,6 +173,14 @@ inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
 }
+
+// Host-side argument checks shared by the entry points (api.cu): the layer
+// configuration, and the subset routing needs (the routing entry points
+// accept configurations whose expert banks are outside the library's limits).
+moe_status_t validate_cfg(const moe_cfg_t* c);
+moe_status_t validate_route_cfg(const moe_cfg_t* c);
+// Records the CUDA error behind a MOE_ERR_CUDA for moe_last_cuda_error.
+void set_last_cuda_error(cudaError_t e);
 
 // One launcher per kernel; each returns the launch's cudaError_t.
 cudaError_t launch_router_logits(const RouterArgs& ra, bool bf16, cudaStream_t st);

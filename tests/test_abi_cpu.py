@@ -136,3 +136,33 @@ def test_gpu_util_configs_are_valid(L):
             cfg = gpu_util.cfg_for(shape, T)
             c = cfg._c()
             assert L.moe_workspace_bytes(ctypes.byref(c)) > 0, shape.name
+
+
+def test_static_route_checks_match_moe_route(L):
+    """moe_route_static returns moe_route's codes for every host-side check
+    (the workspace check aside), and UNSUPPORTED when the logits would not
+    fit its fixed array; none of these touch the device."""
+    fn = L.moe_route_static
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 4 + [ctypes.POINTER(smr._Cfg)] + [ctypes.c_void_p] * 4
+    cases = [dict(top_k=300), dict(router=1, n_group=3), dict(n_experts=1024),
+             dict(n_group=64), dict(router=1, n_group=64, topk_group=1, top_k=2),
+             dict(expert_dtype=7), dict(d_model=100)]
+    for kw in cases:
+        cfg = _cfg(**kw)
+        c = cfg._c()
+        c.workspace = 0x100000
+        c.workspace_bytes = 1 << 40
+        want = L.moe_route(None, None, None, None, ctypes.byref(c), None, None, None, None)
+        got = fn(None, None, None, None, ctypes.byref(cfg._c()), None, None, None, None)
+        assert got == want and got in (1, 2), (kw, got, want)
+    # null and misaligned tensors
+    c = _cfg(T=4)._c()
+    assert fn(None, 0x2000, None, None, ctypes.byref(c), 0x3000, 0x4000, None, None) == 1
+    assert fn(0x2008, 0x2000, None, None, ctypes.byref(c), 0x3000, 0x4000, None, None) == 1
+    # T = 0: nothing to do
+    assert fn(None, None, None, None, ctypes.byref(_cfg(T=0)._c()), None, None, None, None) == 0
+    # T * (E + 1) beyond the fixed array
+    T = (1 << 20) // 257 + 1
+    assert fn(0x2000, 0x2000, None, None, ctypes.byref(_cfg(T=T)._c()), 0x3000, 0x4000,
+              None, None) == 2
