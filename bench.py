@@ -20,7 +20,7 @@ the event nodes do not add to the timed step.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--tokens T]
                        [--workload decode|prefill|deepseek|mixtral]
-                       [--path auto|gemv|tc] [--impl ours|reference]
+                       [--path auto|gemv|tc|fused] [--impl ours|reference]
                        [--no-sweep] [--no-cpu-baseline] [--no-hot-l2] [--breakdown]
 For N > 1 launch with torchrun (one rank per GPU, NCCL): every rank runs an
 independent replica on its own token batch (the layer has no cross-token
@@ -45,6 +45,7 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s (Qwen3.6 shape, T=1..4096); % of HBM/tensor roofline"
 L2_BYTES = 129 * 10 ** 6
 TC_MIN_TOKENS = 6  # the library's MOE_PATH_AUTO switch to the tensor-core path
+FUSED_MAX_TOKENS = 16  # the single-launch decode kernel (--path fused) takes up to this many
 
 WORKLOADS = {
     # name: (preset, default T, description)
@@ -235,12 +236,26 @@ def _cfg(shape, T, path):
         act_dtype=dt[shape.act_dtype], expert_dtype=dt[shape.expert_dtype], path=path)
 
 
+def _uses_fused(shape, T, path):
+    if shape.expert_dtype == "q4" or shape.expert_dtype != shape.act_dtype:
+        return False
+    return path == 3 and T <= FUSED_MAX_TOKENS
+
+
 def _uses_tc(shape, T, path):
     if shape.expert_dtype == "q4":
         return True  # 4-bit banks are dequantised inside the tensor-core kernel
-    if shape.expert_dtype != "bf16":
+    if shape.expert_dtype != "bf16" or _uses_fused(shape, T, path):
         return False
     return path == 2 or (path == 0 and T >= TC_MIN_TOKENS)
+
+
+def _expert_path(shape, T, path):
+    if _uses_fused(shape, T, path):
+        return "single-launch decode kernel"
+    if _uses_tc(shape, T, path):
+        return "tcgen05 grouped GEMM"
+    return "CUDA-core direct-load GEMV" if T <= 8 else "CUDA-core streaming GEMV"
 
 
 class Workload:
@@ -502,7 +517,8 @@ def run_ours(args):
     hbm, tflops, peak_src = _peaks()
     preset, T_default, desc = WORKLOADS[args.workload]
     shape = mi.PRESETS[preset]
-    path = {"auto": smr.PATH_AUTO, "gemv": smr.PATH_GEMV, "tc": smr.PATH_TC}[args.path]
+    path = {"auto": smr.PATH_AUTO, "gemv": smr.PATH_GEMV, "tc": smr.PATH_TC,
+            "fused": smr.PATH_FUSED}[args.path]
     K, W = args.steps, args.warmup
     T = args.tokens or T_default
     weights = Weights(shape, device)
@@ -526,7 +542,9 @@ def run_ours(args):
         duration."""
         wl = Workload(weights, T, _n_copies(shape, T), path)
         tc = _uses_tc(shape, T, path)
-        kern = ("tc_gateup" if tc else "gemv_gateup") if main else None
+        fused = _uses_fused(shape, T, path)
+        kern = ("decode_fused" if fused else ("tc_gateup" if tc else "gemv_gateup")) \
+            if main else None
         sampler = ClockSampler(local) if main else None
         ms, launches, _, (t0, t1), extra = time_graph(wl, K, W, None, sampler,
                                                      N_EXTRA_REPLAYS if main else 0)
@@ -552,7 +570,11 @@ def run_ours(args):
     # roofline of the dominant kernel: bytes and flops per launch, bound by
     # whichever floor is larger
     mean_k = sum(durs) / len(durs) if durs else None
-    gb, gf = gateup_work(shape, T, n_act)
+    if kern == "decode_fused":
+        # the single-launch kernel is the whole layer: its work is the layer's
+        gb, gf = layer_bytes(shape, T, n_act), layer_flops(shape, T)
+    else:
+        gb, gf = gateup_work(shape, T, n_act)
     hbm_bound = gb / (hbm * 1e9) >= gf / (tflops * 1e12)
     if mean_k:
         sec = mean_k * 1e-3
@@ -561,21 +583,23 @@ def run_ours(args):
         ach = None
     peak = hbm if hbm_bound else tflops
     tr = _traffic(kern)
-    roofline = {"kernel": kern + " (routed + shared gate/up + SwiGLU)",
+    roofline = {"kernel": kern + (" (the whole layer in one launch)" if kern == "decode_fused"
+                                  else " (routed + shared gate/up + SwiGLU)"),
                 "bound": "hbm" if hbm_bound else "tensor", "achieved": ach, "peak": peak,
                 "unit": "GB/s" if hbm_bound else "TFLOP/s",
                 "frac": ach / peak if ach else None,
                 "traffic": (tr["dram_bytes_per_unit"] * (n_act + (1 if shape.d_ff_shared else 0))
-                            if tr else None),
+                            if tr and tr.get("unit") != "layer" else
+                            (tr["dram_bytes_per_layer_per_byte"] * gb if tr else None)),
                 "peak_source": peak_src, "algorithmic_bytes_per_launch": gb,
                 "algorithmic_flops_per_launch": gf,
-                "units_per_launch": n_act + (1 if shape.d_ff_shared else 0),
+                "units_per_launch": (1 if kern == "decode_fused" else
+                                     n_act + (1 if shape.d_ff_shared else 0)),
                 "mean_launch_us": mean_k * 1e3 if mean_k else None}
     lb, lf = layer_bytes(shape, T, n_act), layer_flops(shape, T)
     config = dict(workload_config(shape, T, desc))
     config.update({
-              "expert_path": "tcgen05 grouped GEMM" if _uses_tc(shape, T, path)
-              else ("CUDA-core direct-load GEMV" if T <= 8 else "CUDA-core streaming GEMV"),
+              "expert_path": _expert_path(shape, T, path),
               "l2": "weights rotate over %d distinct layer copies (>= 4x L2 per pass)"
                     % len(wl.copies),
               "timing": "one CUDA graph of K steps, replayed once; CUDA events; the dominant "
@@ -658,7 +682,8 @@ def run_eager(args):
     device = torch.device("cuda", 0)
     preset, T_default, desc = WORKLOADS[args.workload]
     shape = mi.PRESETS[preset]
-    path = {"auto": smr.PATH_AUTO, "gemv": smr.PATH_GEMV, "tc": smr.PATH_TC}[args.path]
+    path = {"auto": smr.PATH_AUTO, "gemv": smr.PATH_GEMV, "tc": smr.PATH_TC,
+            "fused": smr.PATH_FUSED}[args.path]
     T = args.tokens or T_default
     wl = Workload(Weights(shape, device), T, 1, path)
     for _ in range(args.eager):
@@ -721,7 +746,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--tokens", type=int, default=0, help="token batch (default: workload's)")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
-    ap.add_argument("--path", choices=["auto", "gemv", "tc"], default="auto")
+    ap.add_argument("--path", choices=["auto", "gemv", "tc", "fused"], default="auto")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

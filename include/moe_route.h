@@ -108,11 +108,19 @@ typedef enum {
                           grouped GEMM for T >= 6 (bf16 experts; 4-bit
                           experts always take the tensor-core path) */
   MOE_PATH_GEMV = 1,   /* CUDA-core weight-streaming GEMV at any T */
-  MOE_PATH_TC = 2      /* tcgen05 grouped GEMM: bf16 or 4-bit experts with bf16
+  MOE_PATH_TC = 2,     /* tcgen05 grouped GEMM: bf16 or 4-bit experts with bf16
                           activations, d_model % 256 == 0, d_ff % 128 == 0,
                           d_ff_shared 0 or == d_ff (4-bit: 0); other shapes
                           return MOE_ERR_UNSUPPORTED (and MOE_PATH_AUTO then
                           uses the GEMV path) */
+  MOE_PATH_FUSED = 3   /* one cooperative launch (one block per SM) for the
+                          whole layer, the device-routed decode of the
+                          Treebeard page's "NVIDIA CUDA path": routing,
+                          expert grouping, gate/up, down and combine as
+                          phases split by two bounded grid barriers.
+                          1 <= T <= 16, bf16 (or fp32) banks and activations
+                          alike, E <= 512, k <= 32; otherwise
+                          MOE_ERR_UNSUPPORTED */
 } moe_path_t;
 
 typedef struct {
@@ -154,7 +162,8 @@ typedef enum {
   MOE_KERNEL_TC_GATEUP = 8,     /* tensor-core grouped gate/up + SwiGLU */
   MOE_KERNEL_TC_DOWN = 9,       /* tensor-core grouped down x alpha */
   MOE_KERNEL_GATHER = 10,       /* packed-row gather of x (tensor-core path) */
-  MOE_KERNEL_TC_ROUTER = 11     /* tensor-core router contraction (T >= 128, bf16) */
+  MOE_KERNEL_TC_ROUTER = 11,    /* tensor-core router contraction (T >= 128, bf16) */
+  MOE_KERNEL_DECODE = 12        /* single-launch decode kernel (MOE_PATH_FUSED) */
 } moe_kernel_t;
 
 /* Returns the ABI version (MOE_ROUTE_ABI_VERSION). */
@@ -182,6 +191,16 @@ MOE_API uint64_t moe_launch_count(void);
 MOE_API moe_status_t moe_trace_kernel(int kernel, void* const* starts, void* const* stops,
                                       int n, int* count);
 
+/* Failure-detection self-test: the next launch of kernel family `kernel`
+ * (MOE_KERNEL_TC_GATEUP, MOE_KERNEL_TC_DOWN or MOE_KERNEL_DECODE) waits on a
+ * flag that nothing sets, and every bounded wait of that launch gives up
+ * after wait_us microseconds instead of about one second. The launch then
+ * records MOE_ERR_DEVICE_TIMEOUT in its workspace's status word, lets its
+ * copies in flight land, frees its tensor memory and returns; the call's
+ * outputs are unspecified. One-shot and process-wide; kernel = 0 disarms.
+ * Returns MOE_ERR_INVALID_ARG for any other kernel family. */
+MOE_API moe_status_t moe_inject_stall(int kernel, uint32_t wait_us);
+
 /* Workspace bytes needed by every call below for this cfg (the workspace
  * fields of cfg are ignored). Returns 0 if cfg is invalid. */
 MOE_API size_t moe_workspace_bytes(const moe_cfg_t* cfg);
@@ -193,7 +212,9 @@ MOE_API moe_status_t moe_workspace_init(const moe_cfg_t* cfg, void* stream);
 /* Synchronises `stream`, reads the workspace's device status word, clears
  * it, and returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_CHECK.
  * If info is non-NULL it receives the raw word (bit 0 bad id, bit 1 wait
- * timeout, upper 16 bits: first failing site). */
+ * timeout, upper 16 bits: first failing site). After a timeout it also
+ * resets every control word of the workspace (a wait that gave up can leave
+ * a grid-barrier count behind), so the workspace is usable again. */
 MOE_API moe_status_t moe_read_device_status(const moe_cfg_t* cfg, void* stream,
                                     uint32_t* info);
 

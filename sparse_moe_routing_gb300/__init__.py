@@ -17,7 +17,8 @@ __all__ = [
     "MoEConfig", "MoEError", "lib", "lib_path", "abi_version", "status_string",
     "workspace_bytes", "alloc_workspace", "route", "bucket", "experts_forward",
     "layer_forward", "read_device_status", "SOFTMAX_TOPK", "SIGMOID_GROUP_TOPK",
-    "F32", "BF16", "Q4_AFFINE_G64", "PATH_AUTO", "PATH_GEMV", "PATH_TC",
+    "F32", "BF16", "Q4_AFFINE_G64", "PATH_AUTO", "PATH_GEMV", "PATH_TC", "PATH_FUSED",
+    "inject_stall",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -25,7 +26,7 @@ lib_path = os.path.join(_PKG, "libmoe_route.so")
 
 SOFTMAX_TOPK, SIGMOID_GROUP_TOPK = 0, 1
 F32, BF16, Q4_AFFINE_G64 = 0, 1, 2
-PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_TC, PATH_FUSED = 0, 1, 2, 3
 _STATUS = ["MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE",
            "MOE_ERR_CUDA", "MOE_ERR_DEVICE_TIMEOUT", "MOE_ERR_DEVICE_CHECK"]
 
@@ -75,12 +76,13 @@ _SIGS = {
     "moe_last_cuda_error": (ctypes.c_char_p, []),
     "moe_trace_kernel": (ctypes.c_int, [ctypes.c_int, _P, _P, ctypes.c_int,
                                         ctypes.POINTER(ctypes.c_int)]),
+    "moe_inject_stall": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint32]),
 }
 
 # kernel families (moe_kernel_t)
 KERNELS = {"router_logits": 1, "router_topk": 2, "shared_gate": 3, "bucket": 4,
            "gemv_gateup": 5, "gemv_down": 6, "combine": 7, "tc_gateup": 8, "tc_down": 9,
-           "gather": 10, "tc_router": 11}
+           "gather": 10, "tc_router": 11, "decode_fused": 12}
 
 _lib = None
 
@@ -223,6 +225,14 @@ def layer_forward(cfg, workspace, x, r_attn, W_router, W_gate, W_up, W_down, out
         _bank(W_down), _ptr(Ws_gate), _ptr(Ws_up), _ptr(Ws_down), _ptr(w_shared),
         ctypes.byref(cfg._c(workspace)), _ptr(out), _ptr(topk_ids), _ptr(weights),
         _stream(stream)), "moe_layer_forward")
+
+
+def inject_stall(kernel: str, wait_us: int):
+    """Failure self-test (moe_inject_stall): the next launch of `kernel`
+    ("tc_gateup", "tc_down" or "decode_fused") waits on a flag nothing sets
+    and gives up after wait_us; None disarms."""
+    _check(lib().moe_inject_stall(0 if kernel is None else KERNELS[kernel], int(wait_us)),
+           "moe_inject_stall")
 
 
 def launch_count() -> int:

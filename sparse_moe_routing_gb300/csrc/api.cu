@@ -62,10 +62,42 @@ bool use_tc(const moe_cfg_t& c) {
   return c.path == MOE_PATH_AUTO && c.T >= kTcMinTokens;
 }
 
+// The single-launch decode kernel runs when asked for (MOE_PATH_FUSED). It
+// is not MOE_PATH_AUTO's choice at any batch size: measured per layer at the
+// Qwen3.6 shape, T=1 40.7 us against 22-24 us for the chain of direct-load
+// GEMV kernels, T=8 145.8 us against 92.5 us for the tensor-core path (its
+// weight stream from shared memory is bound by instruction issue, about
+// 4.5-5 TB/s).
+bool use_fused(const moe_cfg_t& c) {
+  if (c.path != MOE_PATH_FUSED) return false;
+  return decode_fused_supported(c.T, c.d_model, c.n_experts, c.top_k, c.d_ff, c.d_ff_shared,
+                                c.act_dtype, c.expert_dtype);
+}
+
+// Failure self-test state (moe_inject_stall): the kernel family whose next
+// launch stalls, and the wait limit of that launch.
+std::atomic<int> g_stall_kernel{0};
+std::atomic<uint64_t> g_stall_wait_ns{0};
+
+// Takes the one-shot stall for kernel family `kid` if it is armed: returns
+// the wait limit of the launch and sets *stall.
+uint64_t take_stall(int kid, int* stall) {
+  int want = kid;
+  *stall = 0;
+  if (g_stall_kernel.load(std::memory_order_relaxed) == kid &&
+      g_stall_kernel.compare_exchange_strong(want, 0)) {
+    *stall = 1;
+    return g_stall_wait_ns.load();
+  }
+  return kWaitLimitNs;
+}
+
 // Batches of a few tokens on the GEMV path treat every (token, slot) pair
 // as its own group (at most a handful of pairs share an expert), which needs
 // no bucketing pass.
-bool gemv_pairs(const moe_cfg_t& c) { return !use_tc(c) && c.T <= kGemvSmallTokens; }
+bool gemv_pairs(const moe_cfg_t& c) {
+  return !use_tc(c) && !use_fused(c) && c.T <= kGemvSmallTokens;
+}
 
 // Paired GEMM items (two 128-row blocks per B tile) for 4-bit banks whose
 // routed experts average at least two row blocks each: pairing halves the
@@ -132,7 +164,7 @@ moe_status_t validate_cfg(const moe_cfg_t* c) {
   if (c->expert_dtype != MOE_F32 && c->expert_dtype != MOE_BF16 &&
       c->expert_dtype != MOE_Q4_AFFINE_G64)
     return MOE_ERR_INVALID_ARG;
-  if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_TC) return MOE_ERR_INVALID_ARG;
+  if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_FUSED) return MOE_ERR_INVALID_ARG;
   // limits of the library (kernel templates and shared-memory plans)
   if (c->n_experts > 512 || c->top_k > 32) return MOE_ERR_UNSUPPORTED;
   if (c->expert_dtype == MOE_F32 && c->act_dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
@@ -142,6 +174,10 @@ moe_status_t validate_cfg(const moe_cfg_t* c) {
   if ((c->path == MOE_PATH_TC || c->expert_dtype == MOE_Q4_AFFINE_G64) && !tc_shape_ok(*c))
     return MOE_ERR_UNSUPPORTED;
   if (c->expert_dtype == MOE_Q4_AFFINE_G64 && c->path == MOE_PATH_GEMV) return MOE_ERR_UNSUPPORTED;
+  if (c->path == MOE_PATH_FUSED &&
+      !decode_fused_supported(c->T > 0 ? c->T : 1, c->d_model, c->n_experts, c->top_k, c->d_ff,
+                              c->d_ff_shared, c->act_dtype, c->expert_dtype))
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -219,6 +255,7 @@ const char* kernel_name(int kid) {
     case MOE_KERNEL_TC_DOWN: return "moe:tc_down";
     case MOE_KERNEL_GATHER: return "moe:gather";
     case MOE_KERNEL_TC_ROUTER: return "moe:tc_router";
+    case MOE_KERNEL_DECODE: return "moe:decode_fused";
   }
   return "moe:kernel";
 }
@@ -449,6 +486,7 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
   a.n_tiles = I / gu_rows;
   a.bn = gu_bn;
   a.brows_routed = I;
+  a.wait_ns = take_stall(MOE_KERNEL_TC_GATEUP, &a.stall);
   e = run(MOE_KERNEL_TC_GATEUP, st,
           [&] { return launch_tc_gemm(kTcGateUp, m, a, max_rb * a.n_tiles, st); });
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -478,6 +516,7 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
   a.n_tiles = d / 256;
   a.bn = 256;
   a.brows_routed = d;
+  a.wait_ns = take_stall(MOE_KERNEL_TC_DOWN, &a.stall);
   e = run(MOE_KERNEL_TC_DOWN, st,
           [&] { return launch_tc_gemm(kTcDown, m2, a, max_rb * a.n_tiles, st); });
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -543,6 +582,46 @@ moe_status_t enqueue_experts(const void* x, const float* r_attn, const int32_t* 
   return cuda_status(run(MOE_KERNEL_COMBINE, st, [&] { return launch_combine(cb, st); }));
 }
 
+// The single-launch decode kernel: route mode (ids null: the whole layer,
+// writing topk_ids / weights) or given-ids mode (the expert half for the
+// caller's ids, weights and optional shared gate).
+moe_status_t enqueue_fused(const void* x, const float* r_attn, const void* W_router,
+                           const float* bias, const int32_t* ids_in, const float* w_in,
+                           const float* s_in, moe_bank_t Wg, moe_bank_t Wu, moe_bank_t Wd,
+                           const void* Wsg, const void* Wsu, const void* Wsd, const void* w_shared,
+                           const moe_cfg_t* c, float* out, int32_t* ids_out, float* w_out,
+                           cudaStream_t st) {
+  const Plan p = make_plan(*c);
+  DecodeArgs a{};
+  a.x = x;
+  a.r_attn = r_attn;
+  a.W_router = W_router;
+  a.bias = bias;
+  a.w_shared = w_shared;
+  a.ids_in = ids_in;
+  a.w_in = w_in;
+  a.s_in = s_in;
+  a.Wg = Wg.w; a.Wu = Wu.w; a.Wd = Wd.w;
+  a.Wsg = Wsg; a.Wsu = Wsu; a.Wsd = Wsd;
+  a.out = out;
+  a.topk_ids = ids_out;
+  a.weights = w_out;
+  a.logits = at<float>(c, p.logits);
+  a.H = at<float>(c, p.H);
+  a.Hs = at<float>(c, p.Hs);
+  a.ctrl = at<Ctrl>(c, 0);
+  a.T = c->T; a.d = c->d_model; a.E = c->n_experts; a.k = c->top_k;
+  a.I = c->d_ff; a.Is = c->d_ff_shared;
+  a.kind = c->router;
+  a.n_group = c->n_group;
+  a.topk_group = c->topk_group;
+  a.routed_scaling = c->routed_scaling;
+  a.renorm_clamp = c->renorm_clamp;
+  a.wait_ns = take_stall(MOE_KERNEL_DECODE, &a.stall);
+  const bool bf16 = c->act_dtype == MOE_BF16;
+  return cuda_status(run(MOE_KERNEL_DECODE, st, [&] { return launch_decode_fused(a, bf16, st); }));
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -575,7 +654,7 @@ moe_status_t moe_trace_kernel(int kernel, void* const* starts, void* const* stop
     g_trace = TraceState{};
     return MOE_OK;
   }
-  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_TC_ROUTER || n <= 0 || !starts ||
+  if (kernel < MOE_KERNEL_ROUTER_LOGITS || kernel > MOE_KERNEL_DECODE || n <= 0 || !starts ||
       !stops || !count)
     return MOE_ERR_INVALID_ARG;
   g_trace.kernel = kernel;
@@ -584,6 +663,18 @@ moe_status_t moe_trace_kernel(int kernel, void* const* starts, void* const* stop
   g_trace.n = n;
   g_trace.count = count;
   *count = 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_inject_stall(int kernel, uint32_t wait_us) {
+  if (kernel == 0) {
+    g_stall_kernel.store(0);
+    return MOE_OK;
+  }
+  if (kernel != MOE_KERNEL_TC_GATEUP && kernel != MOE_KERNEL_TC_DOWN && kernel != MOE_KERNEL_DECODE)
+    return MOE_ERR_INVALID_ARG;
+  g_stall_wait_ns.store((uint64_t)(wait_us ? wait_us : 1) * 1000ull);
+  g_stall_kernel.store(kernel);
   return MOE_OK;
 }
 
@@ -608,7 +699,11 @@ moe_status_t moe_read_device_status(const moe_cfg_t* cfg, void* stream, uint32_t
   if (cudaMemcpyAsync(&word, cfg->workspace, sizeof(word), cudaMemcpyDeviceToHost, st) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
-  if (cudaMemsetAsync(cfg->workspace, 0, sizeof(word), st) != cudaSuccess) return MOE_ERR_CUDA;
+  // a wait that gave up may leave the grid-barrier and arrival counters
+  // mid-count: after a timeout every control word is reset (no kernel of
+  // this workspace is running once the stream has synchronised)
+  const size_t clear = (word & kDevTimeout) ? sizeof(Ctrl) : sizeof(word);
+  if (cudaMemsetAsync(cfg->workspace, 0, clear, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   if (info) *info = word;
   if (word & kDevTimeout) return MOE_ERR_DEVICE_TIMEOUT;
@@ -674,6 +769,10 @@ moe_status_t moe_experts_forward(const void* x, const float* r_attn, const int32
   }
   if ((const void*)out == x) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
+  if (use_fused(*cfg))
+    return enqueue_fused(x, r_attn, nullptr, nullptr, topk_ids, weights, shared ? s_shared : nullptr,
+                         W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, shared ? w_shared : nullptr,
+                         cfg, out, nullptr, nullptr, st);
   const Plan p = make_plan(*cfg);
   if (shared && !s_shared) {
     // shared gate only: the router with zero routed rows
@@ -719,6 +818,10 @@ moe_status_t moe_layer_forward(const void* x, const float* r_attn, const void* W
   }
   if ((const void*)out == x) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
+  if (use_fused(*cfg))
+    return enqueue_fused(x, r_attn, W_router, expert_bias, nullptr, nullptr, nullptr, W_gate, W_up,
+                         W_down, Ws_gate, Ws_up, Ws_down, shared ? w_shared : nullptr, cfg, out,
+                         topk_ids, weights, st);
   const Plan p = make_plan(*cfg);
   float* s_sh = shared ? at<float>(cfg, p.s_shared) : nullptr;
   s = enqueue_route_bucket(x, W_router, expert_bias, shared ? w_shared : nullptr, cfg, topk_ids,

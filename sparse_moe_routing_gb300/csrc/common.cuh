@@ -26,6 +26,7 @@ enum : uint32_t {
   kSiteTcDown = 6,
   kSiteTcRouter = 7,
   kSiteRouter = 8,
+  kSiteDecode = 9,
 };
 
 struct Ctrl {
@@ -34,7 +35,11 @@ struct Ctrl {
   int32_t n_rowblocks;    // tensor-core path: (group, m-tile) row blocks
   int32_t pad0;
   uint32_t arrive_bucket; // self-resetting arrival counter (multi-CTA bucketing)
-  int32_t pad[59];
+  int32_t pad1;
+  // single-launch decode: grid-barrier arrivals, monotonic (every launch
+  // adds two per block, so it is a multiple of the grid size between launches)
+  unsigned long long grid_arrivals;
+  int32_t pad[56];
 };
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
 
@@ -102,6 +107,15 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Default limit of every bounded on-device wait (about one second).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -1,0 +1,892 @@
+// Single-launch layer forward for decode batches of a few tokens: the whole
+// pipeline of "How Treebeard routes Qwen3.6 MoE tokens" ("Pseudocode": router,
+// routing rule, selected SwiGLU experts weighted by alpha, sigmoid-gated
+// shared expert, residual) in one kernel, with the expert ids kept on the
+// device as in that page's "NVIDIA CUDA path" (device-routed selected-expert
+// mat-vecs). At a few tokens the layer is a stream of weight rows, and a
+// chain of separate launches spends most of its time between kernels; here
+// the steps are phases of one cooperative launch (one block per SM)
+// separated by two bounded grid barriers:
+//
+//  1. routing-independent work spread over the grid: router logits
+//     z = W_router x plus the shared-gate logit w_shared . x (column E) and
+//     the shared expert's gate/up + SwiGLU rows; the shared expert's down
+//     rows each block reads in phase 4 are prefetched into L2;
+//  -- grid barrier --
+//  2. every block applies the routing rule to all tokens itself (the router
+//     kernels' own routing code, and logits summed in their order, so ids
+//     and weights equal moe_route's bit for bit), sorts the (token, slot)
+//     pairs by expert into chunks of at most 8 pairs of one expert, and
+//     prefetches into L2 the routed down rows it reads in phase 4; block 0
+//     writes topk_ids and weights;
+//  3. routed gate/up + SwiGLU: (chunk, row) items in a contiguous range per
+//     block; each weight row is read once per chunk and dotted with every
+//     token of the chunk ("Intel SYCL path": one weight load serves all of
+//     an expert's tokens);
+//  -- grid barrier --
+//  4. down x alpha and the combine: block b owns a range of output columns;
+//     items are (4 columns, chunk); the block then sums, per token and
+//     column, its slots in slot order, the shared expert and the residual
+//     (a fixed order: the result is deterministic).
+//
+// Weight bytes reach the SM through one ring of 4 KB stages per warp: each
+// warp copies the next segments of its own work into its ring with
+// cp.async.bulk (lane 0 issues, completion counted by mbarrier transactions)
+// and computes from shared memory, refilling each stage as soon as it has
+// read it. No register holds a load in flight, so every SM keeps its rings
+// (up to 192 KB) of weights in flight.
+//
+// Every wait is bounded (about one second; a block that gives up records
+// kDevTimeout in the workspace's status word, lets its copies in flight land
+// and returns).
+#include "router_core.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;          // every warp streams and computes
+constexpr int kSB = 4096;                      // bytes per ring stage
+constexpr int kNT = 8;                         // pairs (tokens) per chunk
+constexpr int kDnRows = 4;                     // output columns per phase-4 item
+constexpr int kMaxStages = 4;                  // ring stages per warp, at most
+
+
+// ---------------------------------------------------------------------------
+// mbarriers, bulk copies, bounded waits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n));
+}
+__device__ __forceinline__ void bar_expect(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          su32(dst)),
+      "l"(src), "r"(bytes), "r"(su32(b))
+      : "memory");
+}
+// One L2 prefetch of a contiguous byte range (16-byte aligned start and a
+// multiple of 16 bytes long), in pieces of at most 64 KB.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
+  const char* b = static_cast<const char*>(p);
+  for (size_t o = 0; o < bytes; o += 65536) {
+    const uint32_t n = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b + o), "r"(n) : "memory");
+  }
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+struct Block {
+  uint8_t* ring;
+  uint64_t* full;        // [kWarps * S]
+  volatile int* abort_flag;
+  volatile int* bar_flag;
+  int S;
+  Ctrl* ctrl;
+  uint64_t limit;
+};
+
+// Bounded wait of one lane; on timeout the block's abort flag is raised and
+// the timeout recorded. False once the block is aborting.
+__device__ bool wait_bar(const Block& B, uint64_t* b, uint32_t parity) {
+  if (bar_try(b, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (!bar_try(b, parity)) {
+    if ((++n & 31u) == 0) {
+      if (*B.abort_flag) return false;
+      if (globaltimer_ns() - t0 > B.limit) {
+        *B.abort_flag = 1;
+        report(B.ctrl, kDevTimeout, kSiteDecode);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Ring of warp w: its unit j sits in stage w*S + j%S with parity (j/S)&1.
+__device__ __forceinline__ int stage_of(const Block& B, int w, uint32_t j) {
+  return w * B.S + (int)(j % (uint32_t)B.S);
+}
+
+// The copies that fill one stage: up to kDnRows contiguous pieces.
+struct Copies {
+  const void* src[kDnRows];
+  uint32_t bytes[kDnRows];
+  uint32_t off[kDnRows];
+  int n;
+};
+
+// A warp's unit sequence in one phase: items it, it + step, ... < it1, each
+// cut into segments of `seg` elements of its K; `jn` counts the units issued.
+struct Feed {
+  int it, it1, step, e0;
+  uint32_t jn;
+};
+
+// Issues the warp's next unit (if any) into its stage: describe(it, e0, cp,
+// K, seg) gives the unit's copies, the item's length K and the segment
+// length. Warp-uniform; lane 0 issues.
+template <typename Describe>
+__device__ __forceinline__ void issue(const Block& B, int w, Feed& f, Describe describe, int lane) {
+  if (f.it >= f.it1) return;
+  Copies cp;
+  int K, seg;
+  describe(f.it, f.e0, cp, K, seg);
+  if (lane == 0) {
+    const int st = stage_of(B, w, f.jn);
+    uint32_t total = 0;
+    for (int i = 0; i < cp.n; ++i) total += cp.bytes[i];
+    bar_expect(&B.full[st], total);
+    uint8_t* dst = B.ring + (size_t)st * kSB;
+    for (int i = 0; i < cp.n; ++i) bulk_g2s(dst + cp.off[i], cp.src[i], cp.bytes[i], &B.full[st]);
+  }
+  ++f.jn;
+  f.e0 += seg;
+  if (f.e0 >= K) {
+    f.e0 = 0;
+    f.it += f.step;
+  }
+}
+
+// Waits for the warp's unit j; null once the block is aborting.
+__device__ const uint8_t* acquire(const Block& B, int w, uint32_t j, int lane) {
+  const int st = stage_of(B, w, j);
+  bool ok = lane == 0 ? wait_bar(B, &B.full[st], (j / (uint32_t)B.S) & 1u) : true;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  return ok ? B.ring + (size_t)st * kSB : nullptr;
+}
+// The warp has read its unit j: order those reads before the copy that
+// refills the stage (async proxy), then issue the next unit into it.
+template <typename Refill>
+__device__ __forceinline__ void release(uint32_t& j, Refill& refill) {
+  __syncwarp();
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  refill();
+  ++j;
+}
+
+// ---------------------------------------------------------------------------
+// grid barrier: a 64-bit arrival count that every block increments once per
+// barrier and that never resets; with nb blocks a barrier completes when the
+// count reaches the next multiple of nb (the count is a multiple of nb
+// between launches: each launch adds two per block). One atomic per block;
+// the last arriver is released by its own add.
+// ---------------------------------------------------------------------------
+__device__ bool grid_barrier(const Block& B, bool arrive) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool ok = arrive && !*B.abort_flag;
+    if (ok) {
+      __threadfence();
+      const unsigned long long nb = gridDim.x;
+      const unsigned long long prev = atomicAdd(&B.ctrl->grid_arrivals, 1ull);
+      const unsigned long long target = (prev / nb + 1) * nb;
+      if (prev + 1 != target) {
+        const uint64_t t0 = globaltimer_ns();
+        unsigned n = 0;
+        while ((long long)(ld_acquire_u64(&B.ctrl->grid_arrivals) - target) < 0) {
+          if ((++n & 255u) == 0 && globaltimer_ns() - t0 > B.limit) {
+            ok = false;
+            report(B.ctrl, kDevTimeout, kSiteDecode);
+            break;
+          }
+        }
+      }
+      __threadfence();
+    }
+    *B.bar_flag = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return *B.bar_flag != 0;
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory layout (identical on host and device)
+// ---------------------------------------------------------------------------
+struct Layout {
+  int ring, full, ids, w, key, gpair, cstart, cexp, ssh, misc, y, ystride, bytes;
+};
+__host__ __device__ inline Layout layout(int T, int k, int ncols, int S) {
+  const int P = T * k;
+  Layout L;
+  int o = 0;
+  L.ring = o;   o += kWarps * S * kSB;
+  L.full = o;   o += kWarps * S * 8;
+  L.ids = o;    o += P * 4;
+  L.w = o;      o += P * 4;
+  L.key = o;    o += P * 4;
+  L.gpair = o;  o += P * 4;
+  L.cstart = o; o += (P + 1) * 4;
+  L.cexp = o;   o += P * 4;
+  L.ssh = o;    o += T * 4;
+  L.misc = o;   o += 16;
+  o = (o + 15) & ~15;
+  L.y = o;
+  L.ystride = P + T;
+  o += ncols * L.ystride * 4;
+  L.bytes = o;
+  return L;
+}
+constexpr int kSmemBudget = 227 * 1024 - 1024;
+
+// Output-column quads per block: block b owns quads [b*nq/nb, (b+1)*nq/nb).
+__host__ __device__ inline int quad_lo(int b, int nq, int nb) {
+  return (int)((long long)b * nq / nb);
+}
+__host__ __device__ inline int max_cols(int d, int nb) {
+  const int nq = d / 4;
+  return 4 * ((nq + nb - 1) / nb);
+}
+// Ring stages per warp that fit beside the tables (0: the shape does not fit).
+__host__ __device__ inline int ring_stages(int T, int k, int ncols) {
+  for (int S = kMaxStages; S >= 2; --S)
+    if (layout(T, k, ncols, S).bytes <= kSmemBudget) return S;
+  return 0;
+}
+
+// [lo, hi) of n equal items for this block.
+__device__ __forceinline__ void block_range(int n, int& lo, int& hi) {
+  lo = (int)((long long)blockIdx.x * n / gridDim.x);
+  hi = (int)((long long)(blockIdx.x + 1) * n / gridDim.x);
+}
+
+// ---------------------------------------------------------------------------
+// consumer arithmetic on one stage
+// ---------------------------------------------------------------------------
+// Independent partial sums per dot product, so that a few-token chunk still
+// keeps several FMA chains in flight: 4 for one or two vectors, 2 for four,
+// 1 for eight.
+template <int NJ> struct Parts { static constexpr int v = NJ <= 2 ? 4 : (NJ <= 4 ? 2 : 1); };
+
+// Gate/up stage: gate[seg] at offset 0, up[seg] at offset kSB/2, `len`
+// elements starting at element e0 of the row; accumulates the dot products
+// with tokens tok[0..nj) (acc[2j][.] gate, acc[2j+1][.] up, in partial sums).
+template <typename TW, int NJ>
+__device__ __forceinline__ void gateup_stage(const uint8_t* st, const TW* x, int d, const int* tok,
+                                             int nj, int e0, int len, int lane,
+                                             float (&acc)[2 * NJ][Parts<NJ>::v]) {
+  constexpr int kVec = Chunk<TW>::kVec;
+  constexpr int kP = Parts<NJ>::v;
+  const uint4* g = reinterpret_cast<const uint4*>(st);
+  const uint4* u = reinterpret_cast<const uint4*>(st + kSB / 2);
+  const int nv = len / kVec;
+  for (int c = lane; c < nv; c += 32) {
+    float gf[kVec], uf[kVec];
+    Chunk<TW>::unpack(g[c], gf);
+    Chunk<TW>::unpack(u[c], uf);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (j < nj) {
+        float xf[kVec];
+        Chunk<TW>::unpack(
+            __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok[j] * d + e0) + c), xf);
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          acc[2 * j][e % kP] = fmaf(gf[e], xf[e], acc[2 * j][e % kP]);
+          acc[2 * j + 1][e % kP] = fmaf(uf[e], xf[e], acc[2 * j + 1][e % kP]);
+        }
+      }
+    }
+  }
+}
+
+// Down stage: kDnRows row segments of `len` elements at offsets r * kSB/4;
+// accumulates their dot products with the fp32 vectors h_j (rows hrow[j] of
+// a buffer of row stride hs, written earlier in this launch: read via L2)
+// from element e0 (acc[r * NJ + j][.], in partial sums).
+template <typename TW, int NJ>
+__device__ __forceinline__ void down_stage(const uint8_t* st, const float* h, size_t hs,
+                                           const int* hrow, int nj, int e0, int len, int lane,
+                                           float (&acc)[kDnRows * NJ][Parts<NJ>::v]) {
+  constexpr int kVec = Chunk<TW>::kVec;
+  constexpr int kP = Parts<NJ>::v;
+  const int nv = len / kVec;
+  for (int c = lane; c < nv; c += 32) {
+    float wf[kDnRows][kVec];
+#pragma unroll
+    for (int r = 0; r < kDnRows; ++r)
+      Chunk<TW>::unpack(reinterpret_cast<const uint4*>(st + r * (kSB / kDnRows))[c], wf[r]);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (j < nj) {
+        const float4* hp = reinterpret_cast<const float4*>(h + (size_t)hrow[j] * hs + e0) +
+                           (size_t)c * (kVec / 4);
+        float hf[kVec];
+#pragma unroll
+        for (int q = 0; q < kVec / 4; ++q) {
+          const float4 v = __ldcg(hp + q);
+          hf[4 * q] = v.x; hf[4 * q + 1] = v.y; hf[4 * q + 2] = v.z; hf[4 * q + 3] = v.w;
+        }
+#pragma unroll
+        for (int r = 0; r < kDnRows; ++r)
+#pragma unroll
+          for (int e = 0; e < kVec; ++e)
+            acc[r * NJ + j][e % kP] = fmaf(wf[r][e], hf[e], acc[r * NJ + j][e % kP]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// per-item consumers (one warp; all stages of the item in order)
+// ---------------------------------------------------------------------------
+// Gate/up item: one gate/up row pair dotted with tokens tok[0..nj);
+// h(j) -> out[orow[j] * ostride + r]. False once the block is aborting.
+template <typename TW, int NJ, typename Refill>
+__device__ bool gateup_item(const Block& B, int c, uint32_t& j, Refill& refill, const TW* x, int d,
+                            const int* tok, int nj, float* out, const int* orow, size_t ostride,
+                            int r, int lane) {
+  constexpr int kSeg = kSB / 2 / sizeof(TW);
+  constexpr int kP = Parts<NJ>::v;
+  float part[2 * NJ][kP];
+#pragma unroll
+  for (int i = 0; i < 2 * NJ; ++i)
+#pragma unroll
+    for (int q = 0; q < kP; ++q) part[i][q] = 0.f;
+  for (int e0 = 0; e0 < d; e0 += kSeg) {
+    const uint8_t* st = acquire(B, c, j, lane);
+    if (!st) return false;
+    gateup_stage<TW, NJ>(st, x, d, tok, nj, e0, min(kSeg, d - e0), lane, part);
+    release(j, refill);
+  }
+  float acc[2 * NJ];
+#pragma unroll
+  for (int i = 0; i < 2 * NJ; ++i) {
+    acc[i] = part[i][0];
+#pragma unroll
+    for (int q = 1; q < kP; ++q) acc[i] += part[i][q];
+  }
+  const float sum = reduce_multi<2 * NJ>(acc, lane);
+  constexpr int per = 32 / (2 * NJ);
+  const float up = __shfl_down_sync(0xffffffffu, sum, per);
+  const int idx = lane / per;  // value this lane holds: 2j gate, 2j+1 up
+  if ((lane % per) == 0 && (idx & 1) == 0 && idx / 2 < nj) {
+    int o = orow[0];
+#pragma unroll
+    for (int q = 1; q < NJ; ++q)
+      if (q == idx / 2) o = orow[q];
+    out[(size_t)o * ostride + r] = siluf_(sum) * up;
+  }
+  return true;
+}
+
+// Down item: kDnRows rows (row stride K) dotted with h rows hrow[0..nj); on
+// return lane l < kDnRows * NJ holds the value of (row l / NJ, vector l % NJ).
+template <typename TW, int NJ, typename Refill>
+__device__ bool down_item(const Block& B, int c, uint32_t& j, Refill& refill, int K, const float* h,
+                          size_t hs, const int* hrow, int nj, int lane, float& val) {
+  constexpr int kSeg = kSB / kDnRows / sizeof(TW);
+  constexpr int kP = Parts<NJ>::v;
+  float part[kDnRows * NJ][kP];
+#pragma unroll
+  for (int i = 0; i < kDnRows * NJ; ++i)
+#pragma unroll
+    for (int q = 0; q < kP; ++q) part[i][q] = 0.f;
+  for (int e0 = 0; e0 < K; e0 += kSeg) {
+    const uint8_t* st = acquire(B, c, j, lane);
+    if (!st) return false;
+    down_stage<TW, NJ>(st, h, hs, hrow, nj, e0, min(kSeg, K - e0), lane, part);
+    release(j, refill);
+  }
+  float acc[kDnRows * NJ];
+#pragma unroll
+  for (int i = 0; i < kDnRows * NJ; ++i) {
+    acc[i] = part[i][0];
+#pragma unroll
+    for (int q = 1; q < kP; ++q) acc[i] += part[i][q];
+  }
+  constexpr int NV = kDnRows * NJ;  // 4, 8, 16 or 32: a power of two
+  const float sum = reduce_multi<NV>(acc, lane);   // lane l holds value l / (32 / NV)
+  val = __shfl_sync(0xffffffffu, sum, (lane * (32 / NV)) & 31);
+  return true;
+}
+
+// dispatch on the chunk's pair count (rounded up to 1, 2, 4 or 8)
+template <typename TW, typename Refill>
+__device__ bool gateup_any(const Block& B, int c, uint32_t& j, Refill& refill, const TW* x, int d,
+                           const int* tok, int nj, float* out, const int* orow, size_t ostride,
+                           int r, int lane) {
+  if (nj <= 1)
+    return gateup_item<TW, 1>(B, c, j, refill, x, d, tok, nj, out, orow, ostride, r, lane);
+  if (nj <= 2)
+    return gateup_item<TW, 2>(B, c, j, refill, x, d, tok, nj, out, orow, ostride, r, lane);
+  if (nj <= 4)
+    return gateup_item<TW, 4>(B, c, j, refill, x, d, tok, nj, out, orow, ostride, r, lane);
+  return gateup_item<TW, 8>(B, c, j, refill, x, d, tok, nj, out, orow, ostride, r, lane);
+}
+template <typename TW, typename Refill>
+__device__ bool down_any(const Block& B, int c, uint32_t& j, Refill& refill, int K, const float* h,
+                         size_t hs, const int* hrow, int nj, int lane, float& val, int& njp) {
+  if (nj <= 1) {
+    njp = 1;
+    return down_item<TW, 1>(B, c, j, refill, K, h, hs, hrow, nj, lane, val);
+  }
+  if (nj <= 2) {
+    njp = 2;
+    return down_item<TW, 2>(B, c, j, refill, K, h, hs, hrow, nj, lane, val);
+  }
+  if (nj <= 4) {
+    njp = 4;
+    return down_item<TW, 4>(B, c, j, refill, K, h, hs, hrow, nj, lane, val);
+  }
+  njp = 8;
+  return down_item<TW, 8>(B, c, j, refill, K, h, hs, hrow, nj, lane, val);
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <typename TW, int PL>
+__global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int T = a.T, k = a.k, E = a.E, d = a.d, I = a.I, Is = a.Is;
+  const int P = T * k;
+  const int nb = gridDim.x;
+  const int nq = d / 4;
+  const int q0 = quad_lo(blockIdx.x, nq, nb), q1 = quad_lo(blockIdx.x + 1, nq, nb);
+  const int c0 = 4 * q0, ncols = 4 * (q1 - q0);
+  const int S = ring_stages(T, k, max_cols(d, nb));
+  const Layout Ly = layout(T, k, max_cols(d, nb), S);
+  int* s_ids = reinterpret_cast<int*>(smem + Ly.ids);
+  float* s_w = reinterpret_cast<float*>(smem + Ly.w);
+  int* s_key = reinterpret_cast<int*>(smem + Ly.key);
+  int* s_gpair = reinterpret_cast<int*>(smem + Ly.gpair);
+  int* s_cstart = reinterpret_cast<int*>(smem + Ly.cstart);
+  int* s_cexp = reinterpret_cast<int*>(smem + Ly.cexp);
+  float* s_ssh = reinterpret_cast<float*>(smem + Ly.ssh);
+  volatile int* s_misc = reinterpret_cast<volatile int*>(smem + Ly.misc);  // nch, abort, bar
+  float* s_y = reinterpret_cast<float*>(smem + Ly.y);
+
+  Block B;
+  B.ring = smem + Ly.ring;
+  B.full = reinterpret_cast<uint64_t*>(smem + Ly.full);
+  B.abort_flag = s_misc + 1;
+  B.bar_flag = s_misc + 2;
+  B.S = S;
+  B.ctrl = a.ctrl;
+  B.limit = a.wait_ns;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t jr = 0;  // units this warp has consumed from its ring
+  const bool route = a.ids_in == nullptr;
+  const bool shared = Is > 0;
+  const TW* x = static_cast<const TW*>(a.x);
+  const TW* Wg = static_cast<const TW*>(a.Wg);
+  const TW* Wu = static_cast<const TW*>(a.Wu);
+  const TW* Wd = static_cast<const TW*>(a.Wd);
+  const TW* Wsg = static_cast<const TW*>(a.Wsg);
+  const TW* Wsu = static_cast<const TW*>(a.Wsu);
+  const TW* Wsd = static_cast<const TW*>(a.Wsd);
+  constexpr int kRowSeg = kSB / sizeof(TW);            // logit-row elements per stage
+  constexpr int kPairSeg = kSB / 2 / sizeof(TW);       // gate/up elements per stage
+  constexpr int kDnSeg = kSB / kDnRows / sizeof(TW);   // down-row elements per stage
+
+  // The shared expert's down rows need only phase 1's results: when some
+  // warps have no token to route, they compute this block's shared-expert
+  // columns while the others route (moved out of phase 4).
+  const bool sh_early = shared && T < kWarps;
+  auto down_items = [&](int it0, int it1, int step, int nroute, int nchs) {
+    // items (4-column quad qi, chunk ci): ci < nroute a routed chunk, else a
+    // shared-expert token chunk; results scaled into s_y
+    auto describe = [&](int it, int e0, Copies& cp, int& K, int& seg) {
+      const int qi = it / nchs, ci = it - qi * nchs;
+      const int col = c0 + 4 * qi;
+      const TW* w;
+      if (ci < nroute) {
+        K = I;
+        w = Wd + ((size_t)s_cexp[ci] * d + col) * I;
+      } else {
+        K = Is;
+        w = Wsd + (size_t)col * Is;
+      }
+      seg = kDnSeg;
+      const uint32_t n = (uint32_t)(min(kDnSeg, K - e0) * sizeof(TW));
+      cp.n = kDnRows;
+#pragma unroll
+      for (int rr = 0; rr < kDnRows; ++rr) {
+        cp.src[rr] = w + (size_t)rr * K + e0;
+        cp.bytes[rr] = n;
+        cp.off[rr] = rr * (kSB / kDnRows);
+      }
+    };
+    Feed f{it0, it1, step, 0, jr};
+    auto refill = [&]() { issue(B, warp, f, describe, lane); };
+    for (int i = 0; i < S; ++i) refill();
+    for (int it = it0; it < it1 && !*B.abort_flag; it += step) {
+      const int qi = it / nchs, ci = it - qi * nchs;
+      const int col = c0 + 4 * qi;
+      int hrow[kNT], slot[kNT];
+      int nj, K;
+      const float* h;
+      if (ci < nroute) {
+        const int cs = s_cstart[ci];
+        nj = min(kNT, s_cstart[ci + 1] - cs);
+#pragma unroll
+        for (int q = 0; q < kNT; ++q) hrow[q] = slot[q] = s_gpair[cs + (q < nj ? q : 0)];
+        h = a.H;
+        K = I;
+      } else {
+        const int t0 = (ci - nroute) * kNT;
+        nj = min(kNT, T - t0);
+#pragma unroll
+        for (int q = 0; q < kNT; ++q) {
+          hrow[q] = t0 + (q < nj ? q : 0);
+          slot[q] = P + hrow[q];
+        }
+        h = a.Hs;
+        K = Is;
+      }
+      float v;
+      int njp;
+      if (!down_any<TW>(B, warp, jr, refill, K, h, (size_t)K, hrow, nj, lane, v, njp)) break;
+      const int rr = lane / njp, q = lane - rr * njp;
+      if (rr < kDnRows && q < nj) {
+        int sl = slot[0];
+#pragma unroll
+        for (int z = 1; z < kNT; ++z)
+          if (z == q) sl = slot[z];
+        const float scale = sl < P ? s_w[sl] : s_ssh[sl - P];
+        s_y[(size_t)(col - c0 + rr) * Ly.ystride + sl] = scale * v;
+      }
+    }
+  };
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWarps * S; ++i) bar_init(&B.full[i], 1);
+    s_misc[1] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+
+  // ------------------------------------------------------------- phase 1
+  // logit items (token chunk, row): router rows 0..E-1 (route mode), then the
+  // shared-gate row E when the gate is not given; then shared gate/up items
+  // (token chunk, row). Items are balanced over blocks by their stage count.
+  {
+    const bool slogit = shared && (route || a.s_in == nullptr);
+    int tpc = (int)(32768 / ((size_t)d * sizeof(TW)));  // the router kernel's token chunks
+    tpc = tpc < 1 ? 1 : (tpc > 8 ? 8 : tpc);
+    const int ntc = (T + tpc - 1) / tpc;
+    const int nlr = (route ? E : 0) + (slogit ? 1 : 0);
+    const int nL = nlr * ntc;
+    const int nsh = (T + kNT - 1) / kNT;
+    const int nS = shared ? Is * nsh : 0;
+    const long long cl = (d + kRowSeg - 1) / kRowSeg, cs = (d + kPairSeg - 1) / kPairSeg;
+    const long long ctot = nL * cl + nS * cs;
+    auto first_item = [&](long long cost) -> int {  // first item starting at or after cost
+      if (cost <= nL * cl) return (int)((cost + cl - 1) / cl);
+      return nL + (int)((cost - nL * cl + cs - 1) / cs);
+    };
+    const int lo = first_item(ctot * blockIdx.x / nb);
+    const int hi = first_item(ctot * (blockIdx.x + 1) / nb);
+    if (shared && warp == 0 && lane == 0 && ncols > 0)
+      prefetch_l2(Wsd + (size_t)c0 * Is, (size_t)ncols * Is * sizeof(TW));
+    auto logit_row = [&](int it) -> const TW* {
+      const int r = route ? it / ntc : E;
+      return r < E ? static_cast<const TW*>(a.W_router) + (size_t)r * d
+                   : static_cast<const TW*>(a.w_shared);
+    };
+    auto describe = [&](int it, int e0, Copies& cp, int& K, int& seg) {
+      K = d;
+      if (it < nL) {
+        seg = kRowSeg;
+        cp.n = 1;
+        cp.src[0] = logit_row(it) + e0;
+        cp.bytes[0] = (uint32_t)(min(kRowSeg, d - e0) * sizeof(TW));
+        cp.off[0] = 0;
+      } else {
+        seg = kPairSeg;
+        const int r = (it - nL) % Is;
+        const uint32_t n = (uint32_t)(min(kPairSeg, d - e0) * sizeof(TW));
+        cp.n = 2;
+        cp.src[0] = Wsg + (size_t)r * d + e0;
+        cp.src[1] = Wsu + (size_t)r * d + e0;
+        cp.bytes[0] = cp.bytes[1] = n;
+        cp.off[0] = 0;
+        cp.off[1] = kSB / 2;
+      }
+    };
+    Feed f{lo + warp, hi, kWarps, 0, jr};
+    auto refill = [&]() { issue(B, warp, f, describe, lane); };
+    for (int i = 0; i < S; ++i) refill();
+    const int nvec = d / Chunk<TW>::kVec;
+    for (int it = lo + warp; it < hi && !*B.abort_flag; it += kWarps) {
+      if (it < nL) {
+        const int tc = it % ntc;
+        const int r = route ? it / ntc : E;
+        const int t0 = tc * tpc, nt = min(tpc, T - t0);
+        float acc[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+        bool ok = true;
+        for (int e0 = 0; e0 < d; e0 += kRowSeg) {
+          const uint8_t* st = acquire(B, warp, jr, lane);
+          if (!st) {
+            ok = false;
+            break;
+          }
+          const int cbase = e0 / Chunk<TW>::kVec;
+          auto wl = [&](int cc) { return reinterpret_cast<const uint4*>(st)[cc - cbase]; };
+          router_dots_pass<TW, 8>(wl, reinterpret_cast<const uint4*>(x + (size_t)t0 * d), nvec,
+                                  nt, cbase + lane, acc);
+          release(jr, refill);
+        }
+        if (!ok) break;
+        router_dots_reduce<8>(acc, nt, lane);
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          if (lane == 0 && t < nt) a.logits[(size_t)(t0 + t) * (E + 1) + r] = acc[t];
+      } else {
+        const int sc = (it - nL) / Is, r = (it - nL) - sc * Is;
+        const int t0 = sc * kNT, nj = min(kNT, T - t0);
+        int tok[kNT];
+#pragma unroll
+        for (int q = 0; q < kNT; ++q) tok[q] = t0 + (q < nj ? q : 0);
+        if (!gateup_any<TW>(B, warp, jr, refill, x, d, tok, nj, a.Hs, tok, (size_t)Is, r, lane))
+          break;
+      }
+    }
+  }
+  if (!grid_barrier(B, !(a.stall && blockIdx.x == 0))) goto drain;
+
+  // ------------------------------------------------------------- phase 2
+  if (route) {
+    if (warp < T) {
+      TopkArgs ta{};
+      ta.logits = a.logits;
+      ta.bias = a.kind == MOE_ROUTER_SIGMOID_GROUP_TOPK ? a.bias : nullptr;
+      ta.topk_ids = s_ids;
+      ta.weights = s_w;
+      ta.s_shared = shared ? s_ssh : nullptr;
+      ta.T = T;
+      ta.E = E;
+      ta.k = k;
+      ta.kind = a.kind;
+      ta.n_group = a.n_group;
+      ta.topk_group = a.topk_group;
+      ta.has_shared_logit = shared ? 1 : 0;
+      ta.routed_scaling = a.routed_scaling;
+      ta.renorm_clamp = a.renorm_clamp;
+      topk_token_pl<PL>(ta, warp, lane);
+    }
+  } else {
+    for (int p = threadIdx.x; p < P; p += kThreads) {
+      s_ids[p] = a.ids_in[p];
+      s_w[p] = a.w_in[p];
+    }
+    if (shared) {
+      for (int t = threadIdx.x; t < T; t += kThreads)
+        s_ssh[t] = a.s_in ? a.s_in[t]
+                          : 1.0f / (1.0f + expf(-__ldcg(a.logits + (size_t)t * (E + 1) + E)));
+    }
+  }
+  __syncthreads();
+  if (sh_early && warp >= T) {
+    const int nsh = (T + kNT - 1) / kNT;
+    down_items(warp - T, (q1 - q0) * nsh, kWarps - T, 0, nsh);
+  }
+  if (route && blockIdx.x == 0) {
+    for (int p = threadIdx.x; p < P; p += kThreads) {
+      a.topk_ids[p] = s_ids[p];
+      a.weights[p] = s_w[p];
+    }
+  }
+  // pairs sorted by (expert, pair id); ids outside [0, E) form no chunk
+  for (int p = threadIdx.x; p < P; p += kThreads) {
+    const int e = s_ids[p];
+    const bool ok = e >= 0 && e < E;
+    if (!ok && blockIdx.x == 0) report(a.ctrl, kDevBadId, kSiteDecode);
+    s_key[p] = ok ? e : E;
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += kThreads) {
+    const int key = s_key[p];
+    int rank = 0;
+    for (int q = 0; q < P; ++q) {
+      const int kq = s_key[q];
+      rank += (kq < key || (kq == key && q < p)) ? 1 : 0;
+    }
+    s_gpair[rank] = p;
+  }
+  __syncthreads();
+  // chunks: runs of one expert in the sorted order, cut every kNT pairs
+  if (warp == 0) {
+    int nch = 0, nvalid = 0, run0 = 0;
+    for (int base = 0; base < P; base += 32) {
+      const int r = base + lane;
+      const int key = r < P ? s_key[s_gpair[r]] : E;
+      const int prev = (r > 0 && r < P) ? s_key[s_gpair[r - 1]] : -1;
+      const bool head = r < P && key < E && key != prev;
+      // start of this pair's run: the last head at or before it
+      const unsigned hm = __ballot_sync(0xffffffffu, head);
+      const unsigned below = hm & (0xffffffffu >> (31 - lane));
+      const int my_run0 = below ? base + 31 - __clz(below) : run0;
+      const bool cut = r < P && key < E && ((r - my_run0) % kNT) == 0;
+      const unsigned cm = __ballot_sync(0xffffffffu, cut);
+      if (cut) {
+        const int ch = nch + __popc(cm & ((1u << lane) - 1u));
+        s_cstart[ch] = r;
+        s_cexp[ch] = key;
+      }
+      nch += __popc(cm);
+      nvalid += __popc(__ballot_sync(0xffffffffu, r < P && key < E));
+      run0 = __shfl_sync(0xffffffffu, my_run0, 31);
+    }
+    if (lane == 0) {
+      s_cstart[nch] = nvalid;
+      s_misc[0] = nch;
+    }
+  }
+  __syncthreads();
+  {
+    const int nch = s_misc[0];
+    // the routed down rows this block reads in phase 4, fetched into L2 while
+    // phase 3 streams the gate/up rows (one prefetch per expert)
+    if (ncols > 0) {
+      for (int ch = threadIdx.x; ch < nch; ch += kThreads)
+        if (ch == 0 || s_cexp[ch] != s_cexp[ch - 1])
+          prefetch_l2(Wd + ((size_t)s_cexp[ch] * d + c0) * I, (size_t)ncols * I * sizeof(TW));
+    }
+
+    // ----------------------------------------------------------- phase 3
+    int lo, hi;
+    block_range(nch * I, lo, hi);
+    auto describe = [&](int it, int e0, Copies& cp, int& K, int& seg) {
+      K = d;
+      seg = kPairSeg;
+      const int ch = it / I, r = it - ch * I;
+      const size_t rb = ((size_t)s_cexp[ch] * I + r) * d + e0;
+      const uint32_t n = (uint32_t)(min(kPairSeg, d - e0) * sizeof(TW));
+      cp.n = 2;
+      cp.src[0] = Wg + rb;
+      cp.src[1] = Wu + rb;
+      cp.bytes[0] = cp.bytes[1] = n;
+      cp.off[0] = 0;
+      cp.off[1] = kSB / 2;
+    };
+    Feed f{lo + warp, hi, kWarps, 0, jr};
+    auto refill = [&]() { issue(B, warp, f, describe, lane); };
+    for (int i = 0; i < S; ++i) refill();
+    for (int it = lo + warp; it < hi && !*B.abort_flag; it += kWarps) {
+      const int ch = it / I, r = it - ch * I;
+      const int cs = s_cstart[ch], nj = min(kNT, s_cstart[ch + 1] - cs);
+      int tok[kNT], prow[kNT];
+#pragma unroll
+      for (int q = 0; q < kNT; ++q) {
+        prow[q] = s_gpair[cs + (q < nj ? q : 0)];
+        tok[q] = prow[q] / k;
+      }
+      if (!gateup_any<TW>(B, warp, jr, refill, x, d, tok, nj, a.H, prow, (size_t)I, r, lane))
+        break;
+    }
+  }
+  if (!grid_barrier(B, true)) goto drain;
+
+  // ------------------------------------------------------------- phase 4
+  {
+    const int nch = s_misc[0];
+    const int nsh = (shared && !sh_early) ? (T + kNT - 1) / kNT : 0;
+    down_items(warp, (q1 - q0) * (nch + nsh), kWarps, nch, nch + nsh);
+  }
+  __syncthreads();
+  if (*B.abort_flag) goto drain;
+  // out = r_attn + ((sum over slots, in slot order) + shared)
+  for (int i = threadIdx.x; i < T * ncols; i += kThreads) {
+    const int t = i / ncols, cc = i - t * ncols;
+    const float* yr = s_y + (size_t)cc * Ly.ystride;
+    float acc = 0.f;
+    for (int s = 0; s < k; ++s) {
+      const int p = t * k + s;
+      if (s_key[p] < E) acc += yr[p];
+    }
+    if (shared) acc += yr[P + t];
+    const size_t o = (size_t)t * d + c0 + cc;
+    a.out[o] = a.r_attn[o] + acc;
+  }
+  return;
+
+drain:
+  // a wait gave up (here or in another block): let this block's copies in
+  // flight land before its shared memory is released
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) {
+    }
+  }
+  __syncthreads();
+}
+
+template <typename TW, int PL>
+cudaError_t launch_pl(const DecodeArgs& a, cudaStream_t st) {
+  static int attr[64] = {};
+  const int nb = tc_sm_count();
+  const int ncols = max_cols(a.d, nb);
+  const int S = ring_stages(a.T, a.k, ncols);
+  if (S == 0) return cudaErrorInvalidValue;
+  const Layout L = layout(a.T, a.k, ncols, S);
+  cudaError_t e = ensure_smem_limit(decode_fused_kernel<TW, PL>, L.bytes, attr);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nb);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L.bytes;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, decode_fused_kernel<TW, PL>, a);
+}
+
+template <typename TW>
+cudaError_t launch_tw(const DecodeArgs& a, cudaStream_t st) {
+  if (a.E <= 32) return launch_pl<TW, 1>(a, st);
+  if (a.E <= 64) return launch_pl<TW, 2>(a, st);
+  if (a.E <= 128) return launch_pl<TW, 4>(a, st);
+  if (a.E <= 256) return launch_pl<TW, 8>(a, st);
+  return launch_pl<TW, 16>(a, st);
+}
+
+}  // namespace
+
+bool decode_fused_supported(int T, int d, int E, int k, int I, int Is, int act, int wdt) {
+  if (T < 1 || T > kDecodeMaxTokens || E > 512 || k > 32) return false;
+  if (!((act == MOE_BF16 && wdt == MOE_BF16) || (act == MOE_F32 && wdt == MOE_F32))) return false;
+  if (d % 8 != 0 || I % 8 != 0 || Is % 8 != 0) return false;
+  return ring_stages(T, k, max_cols(d, tc_sm_count())) > 0;
+}
+
+cudaError_t launch_decode_fused(const DecodeArgs& a, bool bf16, cudaStream_t st) {
+  if (a.T == 0) return cudaSuccess;
+  return bf16 ? launch_tw<__nv_bfloat16>(a, st) : launch_tw<float>(a, st);
+}
+
+}  // namespace moe

@@ -77,6 +77,40 @@ struct GemvArgs {
   const int32_t* pair_ids;
 };
 
+// Single-launch decode kernel (decode_fused.cu): the whole layer for a few
+// tokens in one cooperative launch. Route mode (ids_in null): router
+// contraction, routing rule, experts, combine; given-ids mode: the expert
+// half for caller-given ids and weights.
+struct DecodeArgs {
+  const void* x;            // [T][d] act dtype (= weight dtype)
+  const float* r_attn;      // [T][d]
+  const void* W_router;     // [E][d] (route mode)
+  const float* bias;        // [E] or null (sigmoid family)
+  const void* w_shared;     // [d] shared-gate vector (null without a shared expert)
+  const int32_t* ids_in;    // given-ids mode: [T][k]; null in route mode
+  const float* w_in;        // given-ids mode: [T][k]
+  const float* s_in;        // given shared gate [T], or null (computed from w_shared)
+  const void* Wg; const void* Wu; const void* Wd;   // routed banks
+  const void* Wsg; const void* Wsu; const void* Wsd;  // shared expert
+  float* out;               // [T][d]
+  int32_t* topk_ids;        // route mode outputs [T][k]
+  float* weights;
+  float* logits;            // workspace [T][E+1]
+  float* H;                 // workspace [T*k][I] fp32
+  float* Hs;                // workspace [T][Is] fp32
+  Ctrl* ctrl;
+  int T, d, E, k, I, Is;
+  int kind, n_group, topk_group;
+  float routed_scaling, renorm_clamp;
+  uint64_t wait_ns;         // limit of the grid-barrier waits
+  int stall;                // failure self-test: block 0 never arrives at the first barrier
+};
+constexpr int kDecodeMaxTokens = 16;
+// Shapes the single-launch decode kernel takes (T <= kDecodeMaxTokens,
+// f32 or bf16 weights and activations alike, E <= 512, k <= 32).
+bool decode_fused_supported(int T, int d, int E, int k, int I, int Is, int act, int wdt);
+cudaError_t launch_decode_fused(const DecodeArgs& a, bool bf16, cudaStream_t st);
+
 struct CombineArgs {
   const float* r_attn;      // [T][d]
   const float* Y;           // [P][d] f32, or bf16 when y_bf16
@@ -119,6 +153,8 @@ struct TcArgs {
   // box height of the A maps (gate/up and down, bf16): 128, or 64 / 16 when
   // every group holds at most that many rows
   int arows;
+  uint64_t wait_ns;            // limit of every bounded wait (0: about one second)
+  int stall;                   // failure self-test: the MMA warp waits on a flag nothing sets
 };
 
 // The six operand maps: A routed/shared, B0/B1 routed, B2/B3 shared.

@@ -26,43 +26,46 @@ namespace moe {
 // Dot products of one router row with up to KTOK tokens whose activation
 // rows (nvec 16-byte chunks each, consecutive) start at xr (shared or global
 // memory), by one whole warp; afterwards every lane holds the sums acc[t] for
-// t < nt. kU weight chunks per lane are held in registers while the tokens
-// stream past.
-template <typename TA, int KTOK>
-__device__ __forceinline__ void router_row_dots(const TA* wrow, const uint4* xr, int nvec, int nt,
-                                                int lane, float* acc) {
+// t < nt. kRouterU weight chunks per lane are held in registers while the
+// tokens stream past. Split into one pass over kRouterU * 32 chunks
+// (router_dots_pass, weights through a loader wl(c) -> chunk c) and the
+// reduction (router_dots_reduce), so that a caller streaming the row through
+// shared memory in passes of that size gets the same sums bit for bit.
+constexpr int kRouterU = 8;
+
+template <typename TA, int KTOK, typename WL>
+__device__ __forceinline__ void router_dots_pass(WL wl, const uint4* xr, int nvec, int nt, int c0,
+                                                 float* acc) {
   constexpr int kVec = Chunk<TA>::kVec;
-  constexpr int kU = 8;
+  float w[kRouterU][kVec];
 #pragma unroll
-  for (int t = 0; t < KTOK; ++t) acc[t] = 0.f;
-  for (int c0 = lane; c0 < nvec; c0 += 32 * kU) {
-    float w[kU][kVec];
+  for (int u = 0; u < kRouterU; ++u) {
+    const int c = c0 + 32 * u;
+    Chunk<TA>::unpack(c < nvec ? wl(c) : make_uint4(0, 0, 0, 0), w[u]);
+  }
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int c = c0 + 32 * u;
-      Chunk<TA>::unpack(c < nvec ? ldg_stream(wrow + (size_t)c * kVec) : make_uint4(0, 0, 0, 0),
-                        w[u]);
-    }
+  for (int t = 0; t < KTOK; ++t) {
+    if (t < nt) {
+      const uint4* xt = xr + (size_t)t * nvec;
+      uint4 xv[kRouterU];
 #pragma unroll
-    for (int t = 0; t < KTOK; ++t) {
-      if (t < nt) {
-        const uint4* xt = xr + (size_t)t * nvec;
-        uint4 xv[kU];
+      for (int u = 0; u < kRouterU; ++u) {
+        const int c = c0 + 32 * u;
+        xv[u] = c < nvec ? xt[c] : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int c = c0 + 32 * u;
-          xv[u] = c < nvec ? xt[c] : make_uint4(0, 0, 0, 0);
-        }
+      for (int u = 0; u < kRouterU; ++u) {
+        float xf[kVec];
+        Chunk<TA>::unpack(xv[u], xf);
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          float xf[kVec];
-          Chunk<TA>::unpack(xv[u], xf);
-#pragma unroll
-          for (int j = 0; j < kVec; ++j) acc[t] = fmaf(w[u][j], xf[j], acc[t]);
-        }
+        for (int j = 0; j < kVec; ++j) acc[t] = fmaf(w[u][j], xf[j], acc[t]);
       }
     }
   }
+}
+
+template <int KTOK>
+__device__ __forceinline__ void router_dots_reduce(float* acc, int nt, int lane) {
   if (nt == 1) {
     acc[0] = warp_sum(acc[0]);
     return;
@@ -75,6 +78,18 @@ __device__ __forceinline__ void router_row_dots(const TA* wrow, const uint4* xr,
   // lane l holds the total of token l / (32 / NV); gather them to every lane
 #pragma unroll
   for (int t = 0; t < KTOK; ++t) acc[t] = __shfl_sync(0xffffffffu, sum, t * (32 / NV));
+}
+
+template <typename TA, int KTOK>
+__device__ __forceinline__ void router_row_dots(const TA* wrow, const uint4* xr, int nvec, int nt,
+                                                int lane, float* acc) {
+  constexpr int kVec = Chunk<TA>::kVec;
+#pragma unroll
+  for (int t = 0; t < KTOK; ++t) acc[t] = 0.f;
+  auto wl = [&](int c) { return ldg_stream(wrow + (size_t)c * kVec); };
+  for (int c0 = lane; c0 < nvec; c0 += 32 * kRouterU)
+    router_dots_pass<TA, KTOK>(wl, xr, nvec, nt, c0, acc);
+  router_dots_reduce<KTOK>(acc, nt, lane);
 }
 
 // ---------------------------------------------------------------------------

@@ -66,13 +66,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase of `bar` with the given parity; false after ~1 s.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Waits for the phase of `bar` with the given parity; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   uint32_t n = 0;
   while (!mbar_try_wait(bar, parity)) {
-    if ((++n & 63u) == 0 && globaltimer() - t0 > 1000000000ull) return false;
+    if ((++n & 63u) == 0 && globaltimer() - t0 > limit_ns) return false;
   }
   return true;
 }
@@ -382,6 +382,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const uint64_t lim = a.wait_ns ? a.wait_ns : kWaitLimitNs;
   pdl_wait();
   pdl_trigger();
 
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
       const bool two = RB == 2 && (ti.m + 1) * BM < ti.rows;  // second row block present
       const uint32_t item_bytes = stage_bytes + (two ? kStageA : 0);
       for (int kb = 0; kb < nkb; ++kb) {
-        bool ok = lane == 0 ? mbar_wait(&empty[stage], ph ^ 1u) : true;
+        bool ok = lane == 0 ? mbar_wait(&empty[stage], ph ^ 1u, lim) : true;
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
         if (!ok) {
           if (lane == 0) give_up(a, abort_flag, site);
@@ -450,13 +451,23 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
     int stage = 0, acc = 0, bs = 0;
     uint32_t ph = 0, aph = 0, bph = 0;
     bool alive = true;
+    if (a.stall) {
+      // failure self-test: wait on the first accumulator's full barrier,
+      // which only this warp would complete, until the wait gives up
+      bool ok = lane == 0 ? mbar_wait(&tfull[0], 0u, lim) : true;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) give_up(a, abort_flag, site);
+        alive = false;
+      }
+    }
     for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
       bool two = false;
       if (RB == 2) {
         const TileInfo ti = decode_tile<MODE>(a, t, n_rb);
         two = (ti.m + 1) * BM < ti.rows;
       }
-      bool ok = lane == 0 ? mbar_wait(&tempty[acc], aph ^ 1u) : true;
+      bool ok = lane == 0 ? mbar_wait(&tempty[acc], aph ^ 1u, lim) : true;
       ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
       if (!ok) {
         if (lane == 0) give_up(a, abort_flag, site);
@@ -468,10 +479,10 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
         ok = true;
         if (lane == 0) {
           if (Q4) {
-            ok = mbar_wait(&rawfull[stage], ph);     // the A tile of this stage
-            if (ok) ok = mbar_wait(&bfull[bs], bph);  // its dequantised B stage
+            ok = mbar_wait(&rawfull[stage], ph, lim);     // the A tile of this stage
+            if (ok) ok = mbar_wait(&bfull[bs], bph, lim);  // its dequantised B stage
           } else {
-            ok = mbar_wait(&full[stage], ph);
+            ok = mbar_wait(&full[stage], ph, lim);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
@@ -523,7 +534,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
       const TileInfo ti = decode_tile<MODE>(a, t, n_rb);
-      bool ok = lane == 0 ? mbar_wait(&tfull[acc], aph) : true;
+      bool ok = lane == 0 ? mbar_wait(&tfull[acc], aph, lim) : true;
       ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
       if (!ok) {
         if (lane == 0) give_up(a, abort_flag, site);
@@ -660,8 +671,8 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
         }
         bool ok = true;
         if (lane == 0) {
-          ok = mbar_wait(&rawfull[stage], ph);
-          if (ok) ok = mbar_wait(&bempty[bs], bph ^ 1u);
+          ok = mbar_wait(&rawfull[stage], ph, lim);
+          if (ok) ok = mbar_wait(&bempty[bs], bph ^ 1u, lim);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
         if (!ok) {

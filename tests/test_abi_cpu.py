@@ -166,3 +166,12 @@ def test_static_route_checks_match_moe_route(L):
     T = (1 << 20) // 257 + 1
     assert fn(0x2000, 0x2000, None, None, ctypes.byref(_cfg(T=T)._c()), 0x3000, 0x4000,
               None, None) == 2
+
+
+def test_inject_stall_accepts_only_kernels_with_bounded_waits(L):
+    assert L.moe_inject_stall(0, 0) == 0
+    for bad in (1, 2, 4, 7, 11, 99):
+        assert L.moe_inject_stall(bad, 100) == 1
+    for ok in (8, 9, 12):
+        assert L.moe_inject_stall(ok, 100) == 0
+    assert L.moe_inject_stall(0, 0) == 0

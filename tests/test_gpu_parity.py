@@ -191,7 +191,8 @@ def test_bucket_flags_out_of_range_ids(T):
     assert smr.read_device_status(cfg, ws)[0] == 0
 
 
-EXPERT_CASES = [(mi.TINY_F32, 32, 32), (mi.QWEN36, 64, 64), (mi.DEEPSEEK_GROUP, 4096, 16)]
+EXPERT_CASES = [(mi.TINY_F32, 32, 32), (mi.QWEN36, 64, 64), (mi.DEEPSEEK_GROUP, 4096, 16),
+                (mi.QWEN36, 8, 8), (mi.TINY_F32.with_(name="tiny_f32_t3"), 3, 3)]
 
 
 @pytest.mark.parametrize("shape,T,n_check", EXPERT_CASES,
@@ -217,16 +218,21 @@ def test_experts_forward_parity_given_routing(shape, T, n_check):
         assert err <= OUT_TOL[shape.act_dtype], err
 
 
-@pytest.mark.parametrize("shape,T", [(mi.QWEN36, 2), (mi.TINY_F32, 3)], ids=["qwen-T2", "tiny-T3"])
-def test_small_gemv_with_an_expert_repeated_within_a_token(shape, T):
+@pytest.mark.parametrize("path", [smr.PATH_GEMV, smr.PATH_FUSED], ids=["gemv", "fused"])
+@pytest.mark.parametrize("shape,T", [(mi.QWEN36, 2), (mi.TINY_F32, 3), (mi.QWEN36, 16)],
+                         ids=["qwen-T2", "tiny-T3", "qwen-T16"])
+def test_small_batch_with_an_expert_repeated_within_a_token(shape, T, path):
     """Caller-given ids may name one expert in several slots of a token, so an
     expert's group can hold more pairs than the batch has tokens; the
-    direct-load GEMV then walks the group in token chunks."""
+    direct-load GEMV and the single-launch decode kernel then walk the group
+    in chunks of tokens."""
+    if path == smr.PATH_GEMV and T > 8:
+        pytest.skip("the direct-load GEMV takes up to 8 tokens")
     L = layer_host(shape, T)
     dev = DevLayer(shape, L)
     ids, w, s = mi.random_router_outputs(shape, T)
     ids[:, : shape.top_k // 2] = 3          # expert 3 in half the slots of every token
-    cfg = cfg_for(shape, T, smr.PATH_GEMV)
+    cfg = cfg_for(shape, T, path)
     ws = smr.alloc_workspace(cfg)
     sh = dev.shared()
     smr.experts_forward(cfg, ws, dev.t["x"], dev.t["r_attn"], to_dev(ids), to_dev(w),
@@ -238,23 +244,27 @@ def test_small_gemv_with_an_expert_repeated_within_a_token(shape, T):
     assert rel_rms_err(dev.out.cpu().numpy(), ref["out"]) <= OUT_TOL[shape.act_dtype]
 
 
-def test_few_token_gemv_flags_out_of_range_ids():
-    """Batches of a few tokens skip the bucketing pass (each pair is its own
-    group), so the GEMV kernels check the ids themselves: a bad id is flagged
-    in the status word and its pair is skipped, with every access in bounds."""
+@pytest.mark.parametrize("path,site", [(smr.PATH_GEMV, 2), (smr.PATH_FUSED, 9)],
+                         ids=["gemv", "fused"])
+def test_few_token_paths_flag_out_of_range_ids(path, site):
+    """Batches of a few tokens skip the bucketing pass (the direct-load GEMV
+    treats each pair as its own group; the single-launch decode kernel groups
+    pairs itself), so these kernels check the ids themselves: a bad id is
+    flagged in the status word and its pair is skipped, with every access in
+    bounds."""
     shape, T = mi.QWEN36, 2
     L = layer_host(shape, T)
     dev = DevLayer(shape, L)
     ids, w, s = mi.random_router_outputs(shape, T)
     ids[1, 3] = shape.n_experts + 7
-    cfg = cfg_for(shape, T)
+    cfg = cfg_for(shape, T, path)
     ws = smr.alloc_workspace(cfg)
     smr.experts_forward(cfg, ws, dev.t["x"], dev.t["r_attn"], to_dev(ids), to_dev(w),
                         dev.bank("W_gate"), dev.bank("W_up"), dev.bank("W_down"), dev.out,
                         s_shared=to_dev(s), **dev.shared())
     st, word = smr.read_device_status(cfg, ws)
     assert st == smr._STATUS.index("MOE_ERR_DEVICE_CHECK")
-    assert word & 1 and (word >> 16) == 2
+    assert word & 1 and (word >> 16) == site
     # token 0 does not involve the bad pair and is still exact
     ref = orc.moe_experts_forward(L, shape, ids[:1], w[:1].astype(np.float64),
                                   s[:1].astype(np.float64), np.arange(1))
@@ -274,8 +284,9 @@ def test_in_place_residual_update():
     assert torch.equal(dev.t["r_attn"], want)
 
 
-def test_repeat_calls_are_deterministic():
-    shape, T = mi.QWEN36, 64
+@pytest.mark.parametrize("T", [4, 64])
+def test_repeat_calls_are_deterministic(T):
+    shape = mi.QWEN36
     L = layer_host(shape, T)
     dev = DevLayer(shape, L)
     cfg = cfg_for(shape, T)
@@ -293,15 +304,22 @@ CONSISTENCY_CASES = [(mi.QWEN36, 1), (mi.QWEN36, 37), (mi.QWEN36, 64), (mi.DEEPS
                      (mi.TINY_F32, 32), (mi.QWEN36, 600)]
 
 
-@pytest.mark.parametrize("shape,T", CONSISTENCY_CASES,
-                         ids=["%s-T%d" % (c[0].name, c[1]) for c in CONSISTENCY_CASES])
-def test_layer_matches_route_then_experts(shape, T):
+FUSED_CONSISTENCY = [(mi.QWEN36, 1, smr.PATH_FUSED), (mi.QWEN36, 16, smr.PATH_FUSED),
+                     (mi.DEEPSEEK_GROUP, 8, smr.PATH_FUSED),
+                     (mi.TINY_F32.with_(name="tiny_f32_t5"), 5, smr.PATH_FUSED)]
+
+
+@pytest.mark.parametrize("shape,T,path", [c + (smr.PATH_AUTO,) for c in CONSISTENCY_CASES] +
+                         FUSED_CONSISTENCY,
+                         ids=["%s-T%d" % (c[0].name, c[1]) for c in CONSISTENCY_CASES] +
+                         ["%s-T%d-fused" % (c[0].name, c[1]) for c in FUSED_CONSISTENCY])
+def test_layer_matches_route_then_experts(shape, T, path):
     """moe_layer_forward against moe_route followed by moe_experts_forward on
     the same inputs: the same kernels in the same order, so ids, weights and
     the layer output must agree bit for bit."""
     L = layer_host(shape, T)
     dev = DevLayer(shape, L)
-    cfg = cfg_for(shape, T)
+    cfg = cfg_for(shape, T, path)
     ws = smr.alloc_workspace(cfg)
     dev.layer_forward(cfg, ws)
     assert smr.read_device_status(cfg, ws)[0] == 0
@@ -388,12 +406,16 @@ PATH_CASES = [(TC_SMALL, 400), (TC_SMALL, 700), (TC_SMALL, 37), (TC_SMALL, 1), (
               (mi.DEEPSEEK_GROUP, 37)]
 
 
-@pytest.mark.parametrize("path", [smr.PATH_GEMV, smr.PATH_TC], ids=["gemv", "tc"])
+@pytest.mark.parametrize("path", [smr.PATH_GEMV, smr.PATH_TC, smr.PATH_FUSED],
+                         ids=["gemv", "tc", "fused"])
 @pytest.mark.parametrize("shape,T", PATH_CASES,
                          ids=["%s-T%d" % (c[0].name, c[1]) for c in PATH_CASES])
-def test_both_expert_paths_match_oracle(shape, T, path):
-    """The CUDA-core streaming path and the tcgen05 grouped-GEMM path, each
-    forced, against the oracle on every output row."""
+def test_every_expert_path_matches_oracle(shape, T, path):
+    """The CUDA-core streaming path, the tcgen05 grouped-GEMM path and the
+    single-launch decode kernel (batches of up to 16 tokens), each forced,
+    against the oracle on every output row."""
+    if path == smr.PATH_FUSED and T > 16:
+        pytest.skip("the single-launch decode kernel takes up to 16 tokens")
     L, dev, cfg, ws = _run_layer(shape, T, path)
     _check_rows(L, shape, T, dev, "all")
 
