@@ -212,10 +212,10 @@ class Weights:
     """One layer's weights generated once (host), uploaded once, and cloned on
     the device into as many distinct copies as a workload needs."""
 
-    def __init__(self, shape, device):
+    def __init__(self, shape, device, host=None):
         import moe_inputs as mi
         self.shape, self.device = shape, device
-        self.host = mi.make_weights(shape)
+        self.host = mi.make_weights(shape) if host is None else host
         self.copies = [{k: _to_dev(v, device) for k, v in self.host.items()}]
 
     def get(self, n):
@@ -357,6 +357,65 @@ def time_graph(wl, K, W, trace_kernel=None, sampler=None, extra_replays=0):
         extra.append(s.elapsed_time(e))
     del g
     return ms, launches, durs, (t0, t1), extra
+
+
+# The rest of the metric's range (T = 1..4096 and the other configurations),
+# measured in the default run after the decode batches: (workload, tokens).
+SWEEP_WORKLOADS = (("prefill", 4096), ("deepseek", 4096), ("mixtral", 2048),
+                   ("mixtral_q4", 2048))
+
+
+def start_host_weights(names):
+    """Generates the host weights of the sweep's workloads in background
+    threads (numpy's generators release the interpreter lock), so that they
+    are ready when the decode measurements finish."""
+    import concurrent.futures as cf
+    import moe_inputs as mi
+    ex = cf.ThreadPoolExecutor(max_workers=len(names))
+    futs = {n: ex.submit(mi.make_weights, mi.PRESETS[WORKLOADS[n][0]]) for n in names}
+    ex.shutdown(wait=False)
+    return futs
+
+
+def sweep_point(name, T, host, device, local, K, W, hbm, tflops):
+    """One workload of the sweep: the layer timed as a CUDA graph of K steps
+    (weights rotated beyond L2), the clocks during that replay, and the
+    gate/up kernel's mean in-graph duration against its roofline."""
+    import numpy as np
+    import torch
+    import moe_inputs as mi
+    preset, _, desc = WORKLOADS[name]
+    shape = mi.PRESETS[preset]
+    weights = Weights(shape, device, host)
+    wl = Workload(weights, T, _n_copies(shape, T), 0)
+    sampler = ClockSampler(local)
+    ms, _, _, (t0, t1), _ = time_graph(wl, K, W, None, sampler)
+    durs = time_graph(wl, min(K, 100), 3, "tc_gateup")[2]
+    n_act = int(np.unique(wl.ids.cpu().numpy()).size)
+    ms_step = ms / K
+    lb, lf = layer_bytes(shape, T, n_act), layer_flops(shape, T)
+    floor_us = max(lb / (hbm * 1e9), lf / (tflops * 1e12)) * 1e6
+    gb, gf = gateup_work(shape, T, n_act)
+    hbm_bound = gb / (hbm * 1e9) >= gf / (tflops * 1e12)
+    mean_k = sum(durs) / len(durs) if durs else None
+    ach = (gb / (mean_k * 1e-3) / 1e9 if hbm_bound else gf / (mean_k * 1e-3) / 1e12) \
+        if mean_k else None
+    peak = hbm if hbm_bound else tflops
+    out = {"workload": desc % T, "T": T, "us_per_layer": ms_step * 1e3,
+           "tokens_per_s": T / (ms_step * 1e-3), "active_experts": n_act,
+           "layer_floor_us": floor_us, "layer_floor_frac": floor_us / (ms_step * 1e3),
+           "layer_hbm_frac": lb / (ms_step * 1e-3) / 1e9 / hbm,
+           "layer_tensor_frac": lf / (ms_step * 1e-3) / 1e12 / tflops,
+           "dominant": {"kernel": "tc_gateup", "bound": "hbm" if hbm_bound else "tensor",
+                        "mean_launch_us": mean_k * 1e3 if mean_k else None,
+                        "achieved": ach, "peak": peak,
+                        "unit": "GB/s" if hbm_bound else "TFLOP/s",
+                        "frac": ach / peak if ach else None},
+           "clocks": sampler.summary(t0, t1)}
+    del wl, weights
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
 
 def time_e2e(wl, K):
@@ -521,6 +580,9 @@ def run_ours(args):
             "fused": smr.PATH_FUSED}[args.path]
     K, W = args.steps, args.warmup
     T = args.tokens or T_default
+    full_sweep = (not args.no_sweep and args.workload == "decode" and world == 1
+                  and not args.tokens and path == smr.PATH_AUTO)
+    host_futs = start_host_weights([n for n, _ in SWEEP_WORKLOADS]) if full_sweep else {}
     weights = Weights(shape, device)
 
     load = {}
@@ -644,6 +706,13 @@ def run_ours(args):
             if not args.no_hot_l2:
                 sweep[str(Ts)]["hot_l2_ms_per_step"] = hot_l2(Ts)
         config["sweep"] = sweep
+    if full_sweep:
+        # the rest of the metric's range: prefill, the sigmoid-group layer and
+        # the Mixtral-shape layers at their configured batch sizes
+        for name, Tw in SWEEP_WORKLOADS:
+            sweep[name] = sweep_point(name, Tw, host_futs[name].result(), device, local, K, W,
+                                      hbm, tflops)
+            host_futs[name] = None
     if args.breakdown:
         # one more graph replay per kernel family, that family bracketed by
         # events: mean in-graph duration per launch (us)

@@ -116,15 +116,21 @@ PRESETS = {s.name: s for s in (TINY_F32, QWEN36, QWEN36_PREFILL_SKEW,
 # storage encodings
 # ----------------------------------------------------------------------------
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
-    """fp32 -> bf16 bit patterns (uint16), round to nearest, ties to even."""
+    """fp32 -> bf16 bit patterns (uint16), round to nearest, ties to even:
+    add 0x7FFF plus the lowest kept bit, keep the upper half. In 32-bit
+    arithmetic the sum cannot wrap for any finite input (the largest,
+    0xFF7FFFFF + 0x8000, stays below 2^32)."""
     a = np.ascontiguousarray(a, dtype=np.float32)
     out = np.empty(a.shape, dtype=np.uint16)
     flat_in = a.reshape(-1).view(np.uint32)
     flat_out = out.reshape(-1)
     for s in range(0, flat_in.size, _CHUNK):
-        b = flat_in[s:s + _CHUNK].astype(np.uint64)
-        b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
-        flat_out[s:s + _CHUNK] = b.astype(np.uint16)
+        u = flat_in[s:s + _CHUNK]
+        r = (u >> 16) & 1
+        r += 0x7FFF
+        r += u
+        r >>= 16
+        flat_out[s:s + _CHUNK] = r
     return out
 
 
