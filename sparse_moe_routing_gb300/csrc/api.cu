@@ -130,9 +130,13 @@ Plan make_plan(const moe_cfg_t& c) {
   p.pos = take(P * 4);
   p.rowblocks = take(((P + T) / kTcBm + E + 2) * 8);
   p.cta_hist = take((size_t)bucket_ctas((int)P) * E * 4);
-  p.H = take(P * I * 4);
-  p.Hs = take(T * Is * 4);
-  p.Y = take(P * d * 4);
+  // (the single-launch decode kernel's tensor-core variant keeps h in mma
+  // fragment order: up to P chunks, or ceil(T/8) shared chunks, of 8 slots)
+  const bool small = T <= (size_t)kDecodeMaxTokens;
+  p.H = take(small ? P * I * 16 : P * I * 4);
+  const size_t hs_frag = (T + 7) / 8 * Is * 16;
+  p.Hs = take(small && hs_frag > T * Is * 4 ? hs_frag : T * Is * 4);
+  p.Y = take(small && d * (P + T) > P * d ? d * (P + T) * 4 : P * d * 4);
   p.Ys = take(Is ? T * d * 4 : 0);
   p.Xperm = take(tc_shape_ok(c) ? P * d * 2 : 0);
   p.total = off;
@@ -590,9 +594,11 @@ moe_status_t enqueue_fused(const void* x, const float* r_attn, const void* W_rou
                            const float* s_in, moe_bank_t Wg, moe_bank_t Wu, moe_bank_t Wd,
                            const void* Wsg, const void* Wsu, const void* Wsd, const void* w_shared,
                            const moe_cfg_t* c, float* out, int32_t* ids_out, float* w_out,
-                           cudaStream_t st) {
+                           cudaStream_t st, float* s_out = nullptr, bool route_only = false) {
   const Plan p = make_plan(*c);
   DecodeArgs a{};
+  a.route_only = route_only ? 1 : 0;
+  a.s_out = s_out;
   a.x = x;
   a.r_attn = r_attn;
   a.W_router = W_router;
@@ -609,6 +615,7 @@ moe_status_t enqueue_fused(const void* x, const float* r_attn, const void* W_rou
   a.logits = at<float>(c, p.logits);
   a.H = at<float>(c, p.H);
   a.Hs = at<float>(c, p.Hs);
+  a.Yg = at<float>(c, p.Y);
   a.ctrl = at<Ctrl>(c, 0);
   a.T = c->T; a.d = c->d_model; a.E = c->n_experts; a.k = c->top_k;
   a.I = c->d_ff; a.Is = c->d_ff_shared;
@@ -724,6 +731,11 @@ moe_status_t moe_route(const void* x, const void* W_router, const float* expert_
   if (s_shared && (!w_shared || !aligned16(w_shared) || !aligned16(s_shared)))
     return MOE_ERR_INVALID_ARG;
   if (expert_bias && !aligned16(expert_bias)) return MOE_ERR_INVALID_ARG;
+  if (use_fused(*cfg))  // the routing phases of the single-launch kernel
+    return enqueue_fused(x, nullptr, W_router, expert_bias, nullptr, nullptr, nullptr, moe_bank_t{},
+                         moe_bank_t{}, moe_bank_t{}, nullptr, nullptr, nullptr,
+                         s_shared ? w_shared : nullptr, cfg, nullptr, topk_ids, weights,
+                         (cudaStream_t)stream, s_shared, true);
   return enqueue_route(x, W_router, expert_bias, w_shared, cfg, topk_ids, weights, s_shared,
                        (cudaStream_t)stream);
 }

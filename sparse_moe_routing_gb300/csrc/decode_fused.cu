@@ -39,6 +39,9 @@
 // Every wait is bounded (about one second; a block that gives up records
 // kDevTimeout in the workspace's status word, lets its copies in flight land
 // and returns).
+#include <string.h>
+
+#include "decode_mma.cuh"
 #include "router_core.cuh"
 
 namespace moe {
@@ -50,6 +53,27 @@ constexpr int kSB = 4096;                      // bytes per ring stage
 constexpr int kNT = 8;                         // pairs (tokens) per chunk
 constexpr int kDnRows = 4;                     // output columns per phase-4 item
 constexpr int kMaxStages = 4;                  // ring stages per warp, at most
+// Profiling build (-DMOE_DECODE_PHASE_TIMES): thread 0 of every block
+// records the globaltimer at each phase mark i in the control block's spare
+// words, as the earliest and the latest block (u64 pair i at byte 40 + 16 i;
+// the host seeds them with (max, 0) before a call). Marks: 0 start, 1 phase
+// 1 done, 2 past barrier 1, 3 routing rule done, 4 grouping done, 5 phase 3
+// done, 6 past barrier 2, 7 past barrier 3, 8 router tiles done, 9 shared
+// gate/up done, 10 shared-gate row done, 11 down items done.
+#ifdef MOE_DECODE_PHASE_TIMES
+__device__ __forceinline__ void stamp(Ctrl* c, int i) {
+  if (threadIdx.x == 0) {
+    unsigned long long* t = reinterpret_cast<unsigned long long*>(&c->pad[2]);
+    unsigned long long now;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+    atomicMin(&t[2 * i], now);
+    atomicMax(&t[2 * i + 1], now);
+  }
+}
+#define STAMP(i) stamp(a.ctrl, i)
+#else
+#define STAMP(i)
+#endif
 
 
 // ---------------------------------------------------------------------------
@@ -82,14 +106,13 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(su32(b))
       : "memory");
 }
-// One L2 prefetch of a contiguous byte range (16-byte aligned start and a
-// multiple of 16 bytes long), in pieces of at most 64 KB.
-__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
-  const char* b = static_cast<const char*>(p);
-  for (size_t o = 0; o < bytes; o += 65536) {
-    const uint32_t n = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b + o), "r"(n) : "memory");
-  }
+// 2D tile copy (tensor map, coordinates x along the contiguous dimension).
+__device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(su32(bar)), "r"(x), "r"(y)
+      : "memory");
 }
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
   unsigned long long v;
@@ -220,6 +243,9 @@ __device__ bool grid_barrier(const Block& B, bool arrive) {
     *B.bar_flag = ok ? 1 : 0;
   }
   __syncthreads();
+  // data other blocks wrote before the barrier may next be read by bulk
+  // copies (the async proxy)
+  asm volatile("fence.proxy.async;" ::: "memory");
   return *B.bar_flag != 0;
 }
 
@@ -227,14 +253,18 @@ __device__ bool grid_barrier(const Block& B, bool arrive) {
 // shared-memory layout (identical on host and device)
 // ---------------------------------------------------------------------------
 struct Layout {
-  int ring, full, ids, w, key, gpair, cstart, cexp, ssh, misc, y, ystride, bytes;
+  int ring, full, part, ids, w, key, gpair, cstart, cexp, ssh, misc, y, ystride, bytes;
 };
-__host__ __device__ inline Layout layout(int T, int k, int ncols, int S) {
+// Tensor-core variant: cross-warp partial sums of one 16-row block (gate and
+// up, 16 rows x 8 tokens, per warp).
+constexpr int kPartBytes = kWarps * 2 * 16 * 8 * 4;
+__host__ __device__ inline Layout layout(int T, int k, int ncols, int S, bool mma) {
   const int P = T * k;
   Layout L;
   int o = 0;
   L.ring = o;   o += kWarps * S * kSB;
   L.full = o;   o += kWarps * S * 8;
+  L.part = o;   o += mma ? kPartBytes : 0;
   L.ids = o;    o += P * 4;
   L.w = o;      o += P * 4;
   L.key = o;    o += P * 4;
@@ -247,24 +277,30 @@ __host__ __device__ inline Layout layout(int T, int k, int ncols, int S) {
   L.y = o;
   L.ystride = P + T;
   o += ncols * L.ystride * 4;
-  L.bytes = o;
+  L.bytes = o + 1024;  // slack to align the ring to 1024 bytes (swizzled TMA tiles)
   return L;
 }
-constexpr int kSmemBudget = 227 * 1024 - 1024;
+constexpr int kSmemBudget = 227 * 1024;
 
-// Output-column quads per block: block b owns quads [b*nq/nb, (b+1)*nq/nb).
+// Output columns are owned in groups of `gran` (4 on the CUDA cores, 8 for
+// the tensor-core tiles): block b owns groups [b*ng/nb, (b+1)*ng/nb).
 __host__ __device__ inline int quad_lo(int b, int nq, int nb) {
   return (int)((long long)b * nq / nb);
 }
-__host__ __device__ inline int max_cols(int d, int nb) {
-  const int nq = d / 4;
-  return 4 * ((nq + nb - 1) / nb);
+__host__ __device__ inline int max_cols(int d, int nb, int gran) {
+  const int nq = d / gran;
+  return gran * ((nq + nb - 1) / nb);
 }
 // Ring stages per warp that fit beside the tables (0: the shape does not fit).
-__host__ __device__ inline int ring_stages(int T, int k, int ncols) {
+__host__ __device__ inline int ring_stages(int T, int k, int ncols, bool mma) {
   for (int S = kMaxStages; S >= 2; --S)
-    if (layout(T, k, ncols, S).bytes <= kSmemBudget) return S;
+    if (layout(T, k, ncols, S, mma).bytes <= kSmemBudget) return S;
   return 0;
+}
+// The tensor-core variant: bf16, K of the gate/up rows split into 64-wide
+// segments over the 16 warps, 16-row blocks and 128-wide down segments.
+__host__ __device__ inline bool mma_shape(int d, int I, int Is, bool bf16) {
+  return bf16 && d % (64 * kWarps) == 0 && I % 128 == 0 && Is % 128 == 0;
 }
 
 // [lo, hi) of n equal items for this block.
@@ -459,17 +495,42 @@ __device__ bool down_any(const Block& B, int c, uint32_t& j, Refill& refill, int
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <typename TW, int PL>
-__global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+// The tensor maps of the tensor-core variant (128-byte swizzle, 64-wide
+// boxes): gate/up banks [E*I][d] and shared [Is][d] with 16-row boxes, down
+// banks [E*d][I] and shared [d][Is] with 8-row boxes.
+struct DecodeMaps {
+  CUtensorMap g, u, sg, su, dn, sdn, r;  // r: router [E][d]
+};
+
+// A warp's tensor-core down items (see dn_run in the kernel) and the state of
+// its ring feed.
+struct DnPlan {
+  int it0, it1, step, nroute, nchs, obase, nqg, hc0;
+  const uint2* hs;
+};
+struct DnFeed {
+  int fit, fk;
+  uint32_t jn;
+};
+
+template <typename TW, int PL, bool MMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_fused_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUtensorMap mu,
+                        const __grid_constant__ CUtensorMap msg, const __grid_constant__ CUtensorMap msu,
+                        const __grid_constant__ CUtensorMap mdn, const __grid_constant__ CUtensorMap msdn,
+                        const __grid_constant__ CUtensorMap mr, const DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
   const int T = a.T, k = a.k, E = a.E, d = a.d, I = a.I, Is = a.Is;
   const int P = T * k;
   const int nb = gridDim.x;
-  const int nq = d / 4;
+  constexpr int kGran = MMA ? 8 : 4;  // output columns per down item
+  const int nq = d / kGran;
   const int q0 = quad_lo(blockIdx.x, nq, nb), q1 = quad_lo(blockIdx.x + 1, nq, nb);
-  const int c0 = 4 * q0, ncols = 4 * (q1 - q0);
-  const int S = ring_stages(T, k, max_cols(d, nb));
-  const Layout Ly = layout(T, k, max_cols(d, nb), S);
+  const int c0 = kGran * q0, ncols = kGran * (q1 - q0);
+  const int S = ring_stages(T, k, max_cols(d, nb, kGran), MMA);
+  const Layout Ly = layout(T, k, max_cols(d, nb, kGran), S, MMA);
   int* s_ids = reinterpret_cast<int*>(smem + Ly.ids);
   float* s_w = reinterpret_cast<float*>(smem + Ly.w);
   int* s_key = reinterpret_cast<int*>(smem + Ly.key);
@@ -492,7 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t jr = 0;  // units this warp has consumed from its ring
   const bool route = a.ids_in == nullptr;
-  const bool shared = Is > 0;
+  // shared: the shared expert's work; sgate: its gate s_t is computed
+  const bool shared = Is > 0 && !a.route_only;
+  const bool sgate = a.route_only ? a.s_out != nullptr : Is > 0;
   const TW* x = static_cast<const TW*>(a.x);
   const TW* Wg = static_cast<const TW*>(a.Wg);
   const TW* Wu = static_cast<const TW*>(a.Wu);
@@ -507,7 +570,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   // The shared expert's down rows need only phase 1's results: when some
   // warps have no token to route, they compute this block's shared-expert
   // columns while the others route (moved out of phase 4).
-  const bool sh_early = shared && T < kWarps;
+  // (CUDA-core variant; the tensor-core variant keeps them in phase 4,
+  // where they cost no wait on the routing path)
+  const bool sh_early = !MMA && shared && T < kWarps;
   auto down_items = [&](int it0, int it1, int step, int nroute, int nchs) {
     // items (4-column quad qi, chunk ci): ci < nroute a routed chunk, else a
     // shared-expert token chunk; results scaled into s_y
@@ -573,6 +638,275 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       }
     }
   };
+  // Tensor-core down items (bf16): (8-column group qi, chunk ci), one warp
+  // each; the chunk's slots (at most 8) are the A side of mma m16n8k16 and
+  // the 8 columns its n side. Items are numbered column-major (it = qi * nchs
+  // + ci, columns from group obase) or chunk-major (it = ci * nqg + qi).
+  // With hs null a stage holds 8 columns x 128 k of the down bank (two
+  // 64-wide swizzled boxes) and the chunk's h fragments for those k (written
+  // in fragment order by the gate/up items); with hs set, the h fragments of
+  // chunks hc0.. are copied to shared memory once for the whole block
+  // (consecutively, K x 16 bytes each) and a stage holds 8 columns x 256 k
+  // of the bank (four boxes), so that a warp may fill its ring before the h
+  // rows exist.
+  auto dn_decode = [&](const DnPlan& pl, int it, int& qi, int& ci) {
+    if (pl.nqg) {
+      ci = it / pl.nqg;
+      qi = it - ci * pl.nqg;
+    } else {
+      qi = it / pl.nchs;
+      ci = it - qi * pl.nchs;
+    }
+  };
+  auto dn_refill = [&](const DnPlan& pl, DnFeed& f) {
+    if (f.fit >= pl.it1 || *B.abort_flag) return;
+    int qi, ci;
+    dn_decode(pl, f.fit, qi, ci);
+    const int col = 8 * (pl.obase + qi);
+    const bool rt = ci < pl.nroute;
+    const int K = rt ? I : Is;
+    const int nbox = pl.hs ? min(4, (K - f.fk) / 64) : 2;
+    if (lane == 0) {
+      const int st = stage_of(B, warp, f.jn);
+      bar_expect(&B.full[st], pl.hs ? 1024u * nbox : 4096u);
+      uint8_t* dst = B.ring + (size_t)st * kSB;
+      const int y = rt ? s_cexp[ci] * d + col : col;
+      for (int b = 0; b < nbox; ++b)
+        tma2d(dst + 1024 * b, rt ? &mdn : &msdn, &B.full[st], f.fk + 64 * b, y);
+      if (!pl.hs) {
+        const __nv_bfloat16* hf = reinterpret_cast<const __nv_bfloat16*>(rt ? a.H : a.Hs) +
+                                  dmma::frag_index(rt ? ci : ci - pl.nroute, K, 0, f.fk);
+        bulk_g2s(dst + 2048, hf, 2048u, &B.full[st]);
+      }
+    }
+    ++f.jn;
+    f.fk += 64 * nbox;
+    if (f.fk >= K) {
+      f.fk = 0;
+      f.fit += pl.step;
+    }
+  };
+  // fills the warp's ring with the plan's first units
+  auto dn_prime = [&](const DnPlan& pl, DnFeed& f) {
+    f.fit = pl.it0;
+    f.fk = 0;
+    f.jn = jr;
+    for (int i = 0; i < S; ++i) dn_refill(pl, f);
+  };
+  auto dn_run = [&](const DnPlan& pl, DnFeed& f) {
+    auto refill = [&]() { dn_refill(pl, f); };
+    const int g = lane >> 2, t = lane & 3;
+    const int kst = pl.hs ? 256 : 128;  // k per stage
+    for (int it = pl.it0; it < pl.it1 && !*B.abort_flag; it += pl.step) {
+      int qi, ci;
+      dn_decode(pl, it, qi, ci);
+      const int col = 8 * (pl.obase + qi);
+      const bool rt = ci < pl.nroute;
+      const int K = rt ? I : Is;
+      int nj, hrow, slot;
+      if (rt) {
+        const int cs = s_cstart[ci];
+        nj = min(kNT, s_cstart[ci + 1] - cs);
+        hrow = s_gpair[cs + (g < nj ? g : 0)];
+        slot = hrow;
+      } else {
+        const int t0 = (ci - pl.nroute) * kNT;
+        nj = min(kNT, T - t0);
+        hrow = t0 + (g < nj ? g : 0);
+        slot = P + hrow;
+      }
+      const uint2* hc = nullptr;
+      if (pl.hs) {
+        size_t off = 0;
+        for (int c = pl.hc0; c < ci; ++c) off += (size_t)(c < pl.nroute ? I : Is) * 2;
+        hc = pl.hs + off;
+      }
+      float dd[4] = {0.f, 0.f, 0.f, 0.f};
+      bool ok = true;
+      for (int k0 = 0; k0 < K; k0 += kst) {
+        const uint8_t* st = acquire(B, warp, jr, lane);
+        if (!st) {
+          ok = false;
+          break;
+        }
+        const int nbox = pl.hs ? min(4, (K - k0) / 64) : 2;
+        const uint2* af = pl.hs ? hc + (k0 >> 4) * 32 : reinterpret_cast<const uint2*>(st + 2048);
+        dmma::down_tile(st, af, nbox, lane, dd);
+        release(jr, refill);
+      }
+      if (!ok) break;
+      if (g < nj) {
+        const float scale = rt ? s_w[slot] : s_ssh[hrow];
+        a.Yg[(size_t)(col + 2 * t) * Ly.ystride + slot] = scale * dd[0];
+        a.Yg[(size_t)(col + 2 * t + 1) * Ly.ystride + slot] = scale * dd[1];
+      }
+    }
+  };
+  DnPlan pl4{};  // this warp's phase-4 items
+  DnFeed f4{};
+  // Tensor-core gate/up items (bf16), block-wide: item = (chunk, 16-row
+  // block) of a routed expert (sh false: rows of W_gate/W_up, h rows = the
+  // chunk's pairs) or of the shared expert (sh true: token chunk, rows of
+  // Ws_gate/Ws_up, h rows = tokens). Warp w streams the 64-wide K segments
+  // w, w + 16, ... of the item's rows; the 16 partial sums meet in shared
+  // memory and are added in warp order, then SwiGLU gives bf16 h.
+  auto gateup_items_mma = [&](int lo, int hi, bool sh) {
+    const int R = sh ? Is : I;
+    const int nrb = R / 16;
+    const int per = d / 64 / kWarps;  // K segments per warp and item
+    const CUtensorMap* mgp = sh ? &msg : &mg;
+    const CUtensorMap* mup = sh ? &msu : &mu;
+    int fit = lo, fj = 0;
+    uint32_t jn = jr;
+    auto refill = [&]() {
+      if (fit >= hi || *B.abort_flag) return;
+      if (lane == 0) {
+        const int c = fit / nrb, rb = fit - c * nrb;
+        const int y = (sh ? 0 : s_cexp[c] * I) + rb * 16;
+        const int st = stage_of(B, warp, jn);
+        bar_expect(&B.full[st], 4096u);
+        uint8_t* dst = B.ring + (size_t)st * kSB;
+        const int k0 = (warp + kWarps * fj) * 64;
+        tma2d(dst, mgp, &B.full[st], k0, y);
+        tma2d(dst + 2048, mup, &B.full[st], k0, y);
+      }
+      ++jn;
+      if (++fj == per) {
+        fj = 0;
+        ++fit;
+      }
+    };
+    for (int i = 0; i < S; ++i) refill();
+    float* part = reinterpret_cast<float*>(smem + Ly.part);
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(a.x);
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(sh ? a.Hs : a.H);
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t xf0[8], xf1[8];
+    int xc = -1;
+    for (int it = lo; it < hi; ++it) {
+      const int c = it / nrb, rb = it - c * nrb;
+      int nj, cs = 0;
+      if (sh) {
+        nj = min(kNT, T - c * kNT);
+      } else {
+        cs = s_cstart[c];
+        nj = min(kNT, s_cstart[c + 1] - cs);
+      }
+      const bool valid = g < nj;
+      const int tok = sh ? c * kNT + (valid ? g : 0) : s_gpair[cs + (valid ? g : 0)] / k;
+      if (per <= 2 && c != xc) {
+        // the chunk's token fragments for this warp's segments, kept while
+        // the chunk lasts and loaded before its first tile lands
+        dmma::x_frags(xb, d, tok, valid, warp * 64, lane, xf0);
+        if (per == 2) dmma::x_frags(xb, d, tok, valid, (warp + kWarps) * 64, lane, xf1);
+        xc = c;
+      }
+      float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < per; ++j) {
+        uint32_t f[8];
+        if (per <= 2) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = j ? xf1[e] : xf0[e];
+        } else {
+          dmma::x_frags(xb, d, tok, valid, (warp + kWarps * j) * 64, lane, f);
+        }
+        const uint8_t* st = acquire(B, warp, jr, lane);
+        if (!st) break;
+        dmma::gateup_tile(st, f, lane, dg, du);
+        release(jr, refill);
+      }
+      float* pw = part + warp * 256;  // [gate, up][16 rows][8 tokens]
+      pw[g * 8 + 2 * t] = dg[0];
+      pw[g * 8 + 2 * t + 1] = dg[1];
+      pw[(g + 8) * 8 + 2 * t] = dg[2];
+      pw[(g + 8) * 8 + 2 * t + 1] = dg[3];
+      pw[128 + g * 8 + 2 * t] = du[0];
+      pw[128 + g * 8 + 2 * t + 1] = du[1];
+      pw[128 + (g + 8) * 8 + 2 * t] = du[2];
+      pw[128 + (g + 8) * 8 + 2 * t + 1] = du[3];
+      __syncthreads();
+      if (threadIdx.x < 128) {
+        const int r = threadIdx.x >> 3, q = threadIdx.x & 7;
+        float gs = 0.f, us = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+          gs += part[w * 256 + r * 8 + q];
+          us += part[w * 256 + 128 + r * 8 + q];
+        }
+        // h in fragment order for the down items: chunk c, slot q, k = 16 rb + r
+        if (q < nj) out[dmma::frag_index(c, R, q, rb * 16 + r)] = __float2bfloat16_rn(siluf_(gs) * us);
+      }
+      __syncthreads();
+    }
+  };
+  // Tensor-core router contraction (bf16), block-wide: item = (token chunk,
+  // tile of 16 router rows; rows past E read as zeros); the K split and the
+  // warp-ordered sum are those of gateup_items_mma.
+  auto router_items_mma = [&](int lo, int hi, int ntiles) {
+    const int per = d / 64 / kWarps;
+    int fit = lo, fj = 0;
+    uint32_t jn = jr;
+    auto refill = [&]() {
+      if (fit >= hi || *B.abort_flag) return;
+      if (lane == 0) {
+        const int tile = fit % ntiles;
+        const int st = stage_of(B, warp, jn);
+        bar_expect(&B.full[st], 2048u);
+        tma2d(B.ring + (size_t)st * kSB, &mr, &B.full[st], (warp + kWarps * fj) * 64, tile * 16);
+      }
+      ++jn;
+      if (++fj == per) {
+        fj = 0;
+        ++fit;
+      }
+    };
+    for (int i = 0; i < S; ++i) refill();
+    float* part = reinterpret_cast<float*>(smem + Ly.part);
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(a.x);
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t xf0[8], xf1[8];
+    int xc = -1;
+    for (int it = lo; it < hi; ++it) {
+      const int c = it / ntiles, tile = it - c * ntiles;
+      const int nj = min(kNT, T - c * kNT);
+      const bool valid = g < nj;
+      const int tok = c * kNT + (valid ? g : 0);
+      if (per <= 2 && c != xc) {
+        dmma::x_frags(xb, d, tok, valid, warp * 64, lane, xf0);
+        if (per == 2) dmma::x_frags(xb, d, tok, valid, (warp + kWarps) * 64, lane, xf1);
+        xc = c;
+      }
+      float dr[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < per; ++j) {
+        uint32_t f[8];
+        if (per <= 2) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = j ? xf1[e] : xf0[e];
+        } else {
+          dmma::x_frags(xb, d, tok, valid, (warp + kWarps * j) * 64, lane, f);
+        }
+        const uint8_t* st = acquire(B, warp, jr, lane);
+        if (!st) break;
+        dmma::router_tile(st, f, lane, dr);
+        release(jr, refill);
+      }
+      float* pw = part + warp * 256;
+      pw[g * 8 + 2 * t] = dr[0];
+      pw[g * 8 + 2 * t + 1] = dr[1];
+      pw[(g + 8) * 8 + 2 * t] = dr[2];
+      pw[(g + 8) * 8 + 2 * t + 1] = dr[3];
+      __syncthreads();
+      if (threadIdx.x < 128) {
+        const int r = threadIdx.x >> 3, q = threadIdx.x & 7;
+        const int col = tile * 16 + r;
+        if (q < nj && col < E) {
+          float z = 0.f;
+          for (int w = 0; w < kWarps; ++w) z += part[w * 256 + r * 8 + q];
+          a.logits[(size_t)(c * kNT + q) * (E + 1) + col] = z;
+        }
+      }
+      __syncthreads();
+    }
+  };
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWarps * S; ++i) bar_init(&B.full[i], 1);
     s_misc[1] = 0;
@@ -581,20 +915,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   __syncthreads();
   pdl_wait();
   pdl_trigger();
+  STAMP(0);
 
   // ------------------------------------------------------------- phase 1
   // logit items (token chunk, row): router rows 0..E-1 (route mode), then the
   // shared-gate row E when the gate is not given; then shared gate/up items
   // (token chunk, row). Items are balanced over blocks by their stage count.
   {
-    const bool slogit = shared && (route || a.s_in == nullptr);
+    const bool slogit = sgate && (route || a.s_in == nullptr);
     int tpc = (int)(32768 / ((size_t)d * sizeof(TW)));  // the router kernel's token chunks
     tpc = tpc < 1 ? 1 : (tpc > 8 ? 8 : tpc);
     const int ntc = (T + tpc - 1) / tpc;
-    const int nlr = (route ? E : 0) + (slogit ? 1 : 0);
+    // (the tensor-core variant contracts the router rows and the shared-gate
+    // row block-wide below)
+    const int nlr = MMA ? 0 : (route ? E : 0) + (slogit ? 1 : 0);
     const int nL = nlr * ntc;
     const int nsh = (T + kNT - 1) / kNT;
-    const int nS = shared ? Is * nsh : 0;
+    // (the tensor-core variant runs the shared gate/up rows block-wide after
+    // the logit rows, so only the logit rows are balanced here)
+    const int nS = (shared && !MMA) ? Is * nsh : 0;
     const long long cl = (d + kRowSeg - 1) / kRowSeg, cs = (d + kPairSeg - 1) / kPairSeg;
     const long long ctot = nL * cl + nS * cs;
     auto first_item = [&](long long cost) -> int {  // first item starting at or after cost
@@ -603,10 +942,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     };
     const int lo = first_item(ctot * blockIdx.x / nb);
     const int hi = first_item(ctot * (blockIdx.x + 1) / nb);
-    if (shared && warp == 0 && lane == 0 && ncols > 0)
-      prefetch_l2(Wsd + (size_t)c0 * Is, (size_t)ncols * Is * sizeof(TW));
     auto logit_row = [&](int it) -> const TW* {
-      const int r = route ? it / ntc : E;
+      const int r = (route && !MMA) ? it / ntc : E;
       return r < E ? static_cast<const TW*>(a.W_router) + (size_t)r * d
                    : static_cast<const TW*>(a.w_shared);
     };
@@ -637,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     for (int it = lo + warp; it < hi && !*B.abort_flag; it += kWarps) {
       if (it < nL) {
         const int tc = it % ntc;
-        const int r = route ? it / ntc : E;
+        const int r = (route && !MMA) ? it / ntc : E;
         const int t0 = tc * tpc, nt = min(tpc, T - t0);
         float acc[8];
 #pragma unroll
@@ -670,8 +1007,73 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
           break;
       }
     }
+    if constexpr (MMA) {
+      // one list of block-wide items, router tiles of 16 experts first, then
+      // the shared expert's 16-row blocks, cut evenly over the blocks
+      const int nte = route ? (E + 15) / 16 : 0;
+      const int nR = ((T + kNT - 1) / kNT) * nte;
+      const int nSh = shared ? nsh * (Is / 16) : 0;
+      int blo, bhi;
+      block_range(nR + nSh, blo, bhi);
+      // the shared-gate row: K split over all threads of one block with no
+      // item (block 0 when the items do not fill the grid, else the last
+      // block), one accumulator per token, summed in lane order within a
+      // warp and in warp order across warps
+      if (slogit && blockIdx.x == (nR + nSh < nb ? 0 : nb - 1)) {
+        const uint4* wv = reinterpret_cast<const uint4*>(a.w_shared);
+        const uint4* xv = reinterpret_cast<const uint4*>(x);
+        const int nv = d / 8;
+        float acc[kDecodeMaxTokens];
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxTokens; ++t) acc[t] = 0.f;
+        for (int c = threadIdx.x; c < nv; c += kThreads) {
+          float wf[8];
+          Chunk<TW>::unpack(__ldg(wv + c), wf);
+#pragma unroll
+          for (int h = 0; h < kDecodeMaxTokens; h += 8) {
+            if (h < T) {
+              // eight token rows at once (rows past T repeat the last one)
+              uint4 xr[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) xr[u] = __ldg(xv + (size_t)min(h + u, T - 1) * nv + c);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                float xf[8];
+                Chunk<TW>::unpack(xr[u], xf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[h + u] = fmaf(wf[e], xf[e], acc[h + u]);
+              }
+            }
+          }
+        }
+        float* part = reinterpret_cast<float*>(smem + Ly.part);
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxTokens; ++t) {
+          if (t < T) {
+            float v = acc[t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) part[warp * kDecodeMaxTokens + t] = v;
+          }
+        }
+        __syncthreads();
+        if (threadIdx.x < T) {
+          float z = 0.f;
+          for (int w = 0; w < kWarps; ++w) z += part[w * kDecodeMaxTokens + threadIdx.x];
+          a.logits[(size_t)threadIdx.x * (E + 1) + E] = z;
+        }
+        __syncthreads();
+        STAMP(10);
+      }
+      router_items_mma(min(blo, nR), min(bhi, nR), nte);
+      if (blo < nR) STAMP(8);
+      if (shared) gateup_items_mma(max(blo, nR) - nR, max(bhi, nR) - nR, true);
+      if (shared && bhi > nR) STAMP(9);
+    }
   }
+  STAMP(1);
   if (!grid_barrier(B, !(a.stall && blockIdx.x == 0))) goto drain;
+  STAMP(2);
 
   // ------------------------------------------------------------- phase 2
   if (route) {
@@ -681,14 +1083,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       ta.bias = a.kind == MOE_ROUTER_SIGMOID_GROUP_TOPK ? a.bias : nullptr;
       ta.topk_ids = s_ids;
       ta.weights = s_w;
-      ta.s_shared = shared ? s_ssh : nullptr;
+      ta.s_shared = sgate ? s_ssh : nullptr;
       ta.T = T;
       ta.E = E;
       ta.k = k;
       ta.kind = a.kind;
       ta.n_group = a.n_group;
       ta.topk_group = a.topk_group;
-      ta.has_shared_logit = shared ? 1 : 0;
+      ta.has_shared_logit = sgate ? 1 : 0;
       ta.routed_scaling = a.routed_scaling;
       ta.renorm_clamp = a.renorm_clamp;
       topk_token_pl<PL>(ta, warp, lane);
@@ -705,6 +1107,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     }
   }
   __syncthreads();
+  STAMP(3);
   if (sh_early && warp >= T) {
     const int nsh = (T + kNT - 1) / kNT;
     down_items(warp - T, (q1 - q0) * nsh, kWarps - T, 0, nsh);
@@ -714,7 +1117,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       a.topk_ids[p] = s_ids[p];
       a.weights[p] = s_w[p];
     }
+    if (a.route_only && a.s_out)
+      for (int t = threadIdx.x; t < T; t += kThreads) a.s_out[t] = s_ssh[t];
   }
+  if (a.route_only) return;
   // pairs sorted by (expert, pair id); ids outside [0, E) form no chunk
   for (int p = threadIdx.x; p < P; p += kThreads) {
     const int e = s_ids[p];
@@ -764,17 +1170,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   __syncthreads();
   {
     const int nch = s_misc[0];
-    // the routed down rows this block reads in phase 4, fetched into L2 while
-    // phase 3 streams the gate/up rows (one prefetch per expert)
-    if (ncols > 0) {
-      for (int ch = threadIdx.x; ch < nch; ch += kThreads)
-        if (ch == 0 || s_cexp[ch] != s_cexp[ch - 1])
-          prefetch_l2(Wd + ((size_t)s_cexp[ch] * d + c0) * I, (size_t)ncols * I * sizeof(TW));
+    STAMP(4);
+    if constexpr (MMA) {
+      // phase 4's plan: (8-column group, chunk) items over the whole grid,
+      // evenly, chunk-major, so that a block's range touches one or two
+      // chunks, whose h fragments are copied to shared memory once when
+      // they fit; the results go to the workspace and meet after one more
+      // barrier. With h in shared memory the rings are filled before the
+      // barrier.
+      const int nsh = shared ? (T + kNT - 1) / kNT : 0;
+      int lo4, hi4;
+      block_range(nq * (nch + nsh), lo4, hi4);
+      pl4 = DnPlan{lo4 + warp, hi4, kWarps, nch, nch + nsh, 0, nq, 0, nullptr};
+      if (lo4 < hi4) {
+        const int hc0 = lo4 / nq, hc1 = (hi4 - 1) / nq;
+        size_t bytes = 0;
+        for (int c = hc0; c <= hc1; ++c) bytes += (size_t)(c < nch ? I : Is) * 16;
+        if (bytes <= (size_t)kPartBytes) {
+          pl4.hc0 = hc0;
+          pl4.hs = reinterpret_cast<const uint2*>(smem + Ly.part);
+        }
+      }
     }
-
     // ----------------------------------------------------------- phase 3
     int lo, hi;
-    block_range(nch * I, lo, hi);
+    if constexpr (MMA) {
+      block_range(nch * (I / 16), lo, hi);
+      gateup_items_mma(lo, hi, false);
+      lo = hi = 0;  // the per-warp rows below have no work
+    } else {
+      block_range(nch * I, lo, hi);
+    }
     auto describe = [&](int it, int e0, Copies& cp, int& K, int& seg) {
       K = d;
       seg = kPairSeg;
@@ -803,27 +1229,57 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       if (!gateup_any<TW>(B, warp, jr, refill, x, d, tok, nj, a.H, prow, (size_t)I, r, lane))
         break;
     }
+    if constexpr (MMA) {
+      if (pl4.hs) dn_prime(pl4, f4);
+    }
   }
+  STAMP(5);
   if (!grid_barrier(B, true)) goto drain;
+  STAMP(6);
 
   // ------------------------------------------------------------- phase 4
   {
     const int nch = s_misc[0];
     const int nsh = (shared && !sh_early) ? (T + kNT - 1) / kNT : 0;
-    down_items(warp, (q1 - q0) * (nch + nsh), kWarps, nch, nch + nsh);
+    if constexpr (MMA) {
+      if (pl4.hs) {
+        const int lo4 = pl4.it0 - warp, hi4 = pl4.it1;
+        uint4* dst = reinterpret_cast<uint4*>(smem + Ly.part);
+        size_t o = 0;
+        for (int c = lo4 / nq; c <= (hi4 - 1) / nq; ++c) {
+          const bool rt = c < nch;
+          const int K = rt ? I : Is;
+          const uint4* src = reinterpret_cast<const uint4*>(
+              reinterpret_cast<const __nv_bfloat16*>(rt ? a.H : a.Hs) +
+              dmma::frag_index(rt ? c : c - nch, K, 0, 0));
+          for (int i = threadIdx.x; i < K; i += kThreads) dst[o + i] = __ldcg(src + i);
+          o += K;
+        }
+      }
+      __syncthreads();
+      if (!pl4.hs) dn_prime(pl4, f4);
+      dn_run(pl4, f4);
+      STAMP(11);
+    } else {
+      down_items(warp, (q1 - q0) * (nch + nsh), kWarps, nch, nch + nsh);
+    }
+  }
+  if constexpr (MMA) {
+    if (!grid_barrier(B, true)) goto drain;
   }
   __syncthreads();
+  STAMP(7);
   if (*B.abort_flag) goto drain;
   // out = r_attn + ((sum over slots, in slot order) + shared)
   for (int i = threadIdx.x; i < T * ncols; i += kThreads) {
     const int t = i / ncols, cc = i - t * ncols;
-    const float* yr = s_y + (size_t)cc * Ly.ystride;
+    const float* yr = (MMA ? a.Yg + (size_t)c0 * Ly.ystride : s_y) + (size_t)cc * Ly.ystride;
     float acc = 0.f;
     for (int s = 0; s < k; ++s) {
       const int p = t * k + s;
-      if (s_key[p] < E) acc += yr[p];
+      if (s_key[p] < E) acc += MMA ? __ldcg(yr + p) : yr[p];
     }
-    if (shared) acc += yr[P + t];
+    if (shared) acc += MMA ? __ldcg(yr + P + t) : yr[P + t];
     const size_t o = (size_t)t * d + c0 + cc;
     a.out[o] = a.r_attn[o] + acc;
   }
@@ -841,16 +1297,29 @@ drain:
   __syncthreads();
 }
 
-template <typename TW, int PL>
+template <typename TW, int PL, bool MMA>
 cudaError_t launch_pl(const DecodeArgs& a, cudaStream_t st) {
   static int attr[64] = {};
   const int nb = tc_sm_count();
-  const int ncols = max_cols(a.d, nb);
-  const int S = ring_stages(a.T, a.k, ncols);
+  const int ncols = max_cols(a.d, nb, MMA ? 8 : 4);
+  const int S = ring_stages(a.T, a.k, ncols, MMA);
   if (S == 0) return cudaErrorInvalidValue;
-  const Layout L = layout(a.T, a.k, ncols, S);
-  cudaError_t e = ensure_smem_limit(decode_fused_kernel<TW, PL>, L.bytes, attr);
+  const Layout L = layout(a.T, a.k, ncols, S, MMA);
+  cudaError_t e = ensure_smem_limit(decode_fused_kernel<TW, PL, MMA>, L.bytes, attr);
   if (e != cudaSuccess) return e;
+  DecodeMaps m;
+  memset(&m, 0, sizeof(m));
+  if (MMA) {
+    const uint64_t E = a.E, I = a.I, d = a.d, Is = a.Is;
+    bool ok = a.route_only ||
+              (tc_make_map(&m.g, a.Wg, E * I, d, 16) && tc_make_map(&m.u, a.Wu, E * I, d, 16) &&
+               tc_make_map(&m.dn, a.Wd, E * d, I, 8));
+    if (ok && Is > 0 && !a.route_only)
+      ok = tc_make_map(&m.sg, a.Wsg, Is, d, 16) && tc_make_map(&m.su, a.Wsu, Is, d, 16) &&
+           tc_make_map(&m.sdn, a.Wsd, d, Is, 8);
+    if (ok && a.W_router) ok = tc_make_map(&m.r, a.W_router, E, d, 16);
+    if (!ok) return cudaErrorInvalidValue;
+  }
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeCooperative;
   at[0].val.cooperative = 1;
@@ -863,16 +1332,17 @@ cudaError_t launch_pl(const DecodeArgs& a, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, decode_fused_kernel<TW, PL>, a);
+  return cudaLaunchKernelEx(&cfg, decode_fused_kernel<TW, PL, MMA>, m.g, m.u, m.sg, m.su, m.dn,
+                            m.sdn, m.r, a);
 }
 
-template <typename TW>
+template <typename TW, bool MMA>
 cudaError_t launch_tw(const DecodeArgs& a, cudaStream_t st) {
-  if (a.E <= 32) return launch_pl<TW, 1>(a, st);
-  if (a.E <= 64) return launch_pl<TW, 2>(a, st);
-  if (a.E <= 128) return launch_pl<TW, 4>(a, st);
-  if (a.E <= 256) return launch_pl<TW, 8>(a, st);
-  return launch_pl<TW, 16>(a, st);
+  if (a.E <= 32) return launch_pl<TW, 1, MMA>(a, st);
+  if (a.E <= 64) return launch_pl<TW, 2, MMA>(a, st);
+  if (a.E <= 128) return launch_pl<TW, 4, MMA>(a, st);
+  if (a.E <= 256) return launch_pl<TW, 8, MMA>(a, st);
+  return launch_pl<TW, 16, MMA>(a, st);
 }
 
 }  // namespace
@@ -881,12 +1351,15 @@ bool decode_fused_supported(int T, int d, int E, int k, int I, int Is, int act, 
   if (T < 1 || T > kDecodeMaxTokens || E > 512 || k > 32) return false;
   if (!((act == MOE_BF16 && wdt == MOE_BF16) || (act == MOE_F32 && wdt == MOE_F32))) return false;
   if (d % 8 != 0 || I % 8 != 0 || Is % 8 != 0) return false;
-  return ring_stages(T, k, max_cols(d, tc_sm_count())) > 0;
+  const bool mma = mma_shape(d, I, Is, act == MOE_BF16);
+  return ring_stages(T, k, max_cols(d, tc_sm_count(), mma ? 8 : 4), mma) > 0;
 }
 
 cudaError_t launch_decode_fused(const DecodeArgs& a, bool bf16, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
-  return bf16 ? launch_tw<__nv_bfloat16>(a, st) : launch_tw<float>(a, st);
+  if (!bf16) return launch_tw<float, false>(a, st);
+  if (mma_shape(a.d, a.I, a.Is, true)) return launch_tw<__nv_bfloat16, true>(a, st);
+  return launch_tw<__nv_bfloat16, false>(a, st);
 }
 
 }  // namespace moe

@@ -98,12 +98,15 @@ struct DecodeArgs {
   float* logits;            // workspace [T][E+1]
   float* H;                 // workspace [T*k][I] fp32
   float* Hs;                // workspace [T][Is] fp32
+  float* Yg;                // workspace [d][T*k + T]: per-column slot results (tensor-core variant)
   Ctrl* ctrl;
   int T, d, E, k, I, Is;
   int kind, n_group, topk_group;
   float routed_scaling, renorm_clamp;
   uint64_t wait_ns;         // limit of the grid-barrier waits
   int stall;                // failure self-test: block 0 never arrives at the first barrier
+  int route_only;           // 1: routing only (moe_route): logits, rule, topk_ids / weights
+  float* s_out;             // route only: the shared gate [T], or null
 };
 constexpr int kDecodeMaxTokens = 16;
 // Shapes the single-launch decode kernel takes (T <= kDecodeMaxTokens,
