@@ -44,7 +44,7 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s (Qwen3.6 shape, T=1..4096); % of HBM/tensor roofline"
 L2_BYTES = 129 * 10 ** 6
-TC_MIN_TOKENS = 6  # the library's MOE_PATH_AUTO switch to the tensor-core path
+TC_MIN_TOKENS = 6  # the library's MOE_PATH_AUTO switch away from the GEMV chain
 FUSED_MAX_TOKENS = 16  # the single-launch decode kernel (--path fused) takes up to this many
 
 WORKLOADS = {
@@ -236,9 +236,18 @@ def _cfg(shape, T, path):
         act_dtype=dt[shape.act_dtype], expert_dtype=dt[shape.expert_dtype], path=path)
 
 
+def _fused_mma(shape):
+    """Whether the single-launch kernel's tensor-core variant takes the shape."""
+    return (shape.expert_dtype == "bf16" and shape.act_dtype == "bf16"
+            and shape.d_model % 1024 == 0 and shape.d_ff % 128 == 0
+            and shape.d_ff_shared % 128 == 0)
+
+
 def _uses_fused(shape, T, path):
     if shape.expert_dtype == "q4" or shape.expert_dtype != shape.act_dtype:
         return False
+    if path == 0:  # the library's automatic choice
+        return TC_MIN_TOKENS <= T <= FUSED_MAX_TOKENS and _fused_mma(shape)
     return path == 3 and T <= FUSED_MAX_TOKENS
 
 

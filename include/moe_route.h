@@ -104,9 +104,14 @@ typedef enum {
 
 /* Expert-path selection for moe_layer_forward / moe_experts_forward. */
 typedef enum {
-  MOE_PATH_AUTO = 0,   /* by shape: CUDA-core GEMV for T <= 5, tensor-core
-                          grouped GEMM for T >= 6 (bf16 experts; 4-bit
-                          experts always take the tensor-core path) */
+  MOE_PATH_AUTO = 0,   /* by shape: CUDA-core GEMV for T <= 5; for T >= 6
+                          with bf16 experts the single launch of
+                          MOE_PATH_FUSED up to T = 16 when its tensor-core
+                          variant takes the shape (d_model % 1024 == 0,
+                          d_ff and d_ff_shared % 128 == 0), else the
+                          tensor-core grouped GEMM; 4-bit experts always
+                          take the tensor-core path. moe_route follows the
+                          same choice for its routing kernels. */
   MOE_PATH_GEMV = 1,   /* CUDA-core weight-streaming GEMV at any T */
   MOE_PATH_TC = 2,     /* tcgen05 grouped GEMM: bf16 or 4-bit experts with bf16
                           activations, d_model % 256 == 0, d_ff % 128 == 0,
@@ -117,10 +122,14 @@ typedef enum {
                           whole layer, the device-routed decode of the
                           Treebeard page's "NVIDIA CUDA path": routing,
                           expert grouping, gate/up, down and combine as
-                          phases split by two bounded grid barriers.
+                          phases split by bounded grid barriers (bf16
+                          shapes as above contract on tensor cores with
+                          mma.sync; others stream on CUDA cores).
                           1 <= T <= 16, bf16 (or fp32) banks and activations
                           alike, E <= 512, k <= 32; otherwise
-                          MOE_ERR_UNSUPPORTED */
+                          MOE_ERR_UNSUPPORTED. moe_route with this path
+                          runs the kernel's routing phases only, so that
+                          its ids and weights are those of the layer. */
 } moe_path_t;
 
 typedef struct {

@@ -21,7 +21,7 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct Plan {
   size_t ctrl, logits, s_shared, counts, offsets, active, perm, pos, rowblocks, cta_hist;
-  size_t H, Hs, Y, Ys, Xperm, total;
+  size_t H, Hs, Y, Ys, Xperm, Gs, total;
 };
 
 // Token batches at or above this size take the tensor-core path under
@@ -56,22 +56,31 @@ int tc_router_bn(const moe_cfg_t& c) {
   return (c.T <= 1024 || c.n_experts % 64 != 0) ? 32 : 64;
 }
 
+// The single-launch decode kernel runs when asked for (MOE_PATH_FUSED), and
+// is MOE_PATH_AUTO's choice for kTcMinTokens..kDecodeMaxTokens tokens when
+// its tensor-core variant takes the shape (bf16). Measured per layer at the
+// Qwen3.6 shape (single launch / tensor-core path / direct-load GEMV chain):
+// T=1 31 / - / 22 us, T=2 43 / - / 35 us, T=4 57 / - / 58 us, T=8 80 / 93 /
+// - us, T=12 115 / 125 / - us, T=16 133 / 143 / - us. Below kTcMinTokens
+// the GEMV chain stays: its launches cost less than the kernel's three grid
+// barriers and in-kernel routing.
+bool fused_ok(const moe_cfg_t& c) {
+  return decode_fused_supported(c.T, c.d_model, c.n_experts, c.top_k, c.d_ff, c.d_ff_shared,
+                                c.act_dtype, c.expert_dtype);
+}
+bool auto_fused(const moe_cfg_t& c) {
+  return c.path == MOE_PATH_AUTO && c.T >= kTcMinTokens && c.T <= kDecodeMaxTokens &&
+         c.act_dtype == MOE_BF16 && c.expert_dtype == MOE_BF16 &&
+         decode_fused_mma(c.d_model, c.d_ff, c.d_ff_shared) && fused_ok(c);
+}
+bool use_fused(const moe_cfg_t& c) {
+  return (c.path == MOE_PATH_FUSED && fused_ok(c)) || auto_fused(c);
+}
+
 bool use_tc(const moe_cfg_t& c) {
   if (!tc_shape_ok(c)) return false;
   if (c.path == MOE_PATH_TC || c.expert_dtype == MOE_Q4_AFFINE_G64) return true;
-  return c.path == MOE_PATH_AUTO && c.T >= kTcMinTokens;
-}
-
-// The single-launch decode kernel runs when asked for (MOE_PATH_FUSED). It
-// is not MOE_PATH_AUTO's choice at any batch size: measured per layer at the
-// Qwen3.6 shape, T=1 40.7 us against 22-24 us for the chain of direct-load
-// GEMV kernels, T=8 145.8 us against 92.5 us for the tensor-core path (its
-// weight stream from shared memory is bound by instruction issue, about
-// 4.5-5 TB/s).
-bool use_fused(const moe_cfg_t& c) {
-  if (c.path != MOE_PATH_FUSED) return false;
-  return decode_fused_supported(c.T, c.d_model, c.n_experts, c.top_k, c.d_ff, c.d_ff_shared,
-                                c.act_dtype, c.expert_dtype);
+  return c.path == MOE_PATH_AUTO && c.T >= kTcMinTokens && !auto_fused(c);
 }
 
 // Failure self-test state (moe_inject_stall): the kernel family whose next
@@ -121,7 +130,8 @@ Plan make_plan(const moe_cfg_t& c) {
   const size_t T = c.T, E = c.n_experts, P = (size_t)c.T * c.top_k;
   const size_t d = c.d_model, I = c.d_ff, Is = c.d_ff_shared;
   p.ctrl = take(sizeof(Ctrl));
-  p.logits = take(T * (E + 1) * 4);
+  const bool small = T <= (size_t)kDecodeMaxTokens;
+  p.logits = take(T * (E + 1) * 4 * (small ? kDecodeKSplit : 1));
   p.s_shared = take(T * 4);
   p.counts = take(E * 4);
   p.offsets = take((E + 1) * 4);
@@ -132,13 +142,13 @@ Plan make_plan(const moe_cfg_t& c) {
   p.cta_hist = take((size_t)bucket_ctas((int)P) * E * 4);
   // (the single-launch decode kernel's tensor-core variant keeps h in mma
   // fragment order: up to P chunks, or ceil(T/8) shared chunks, of 8 slots)
-  const bool small = T <= (size_t)kDecodeMaxTokens;
   p.H = take(small ? P * I * 16 : P * I * 4);
   const size_t hs_frag = (T + 7) / 8 * Is * 16;
   p.Hs = take(small && hs_frag > T * Is * 4 ? hs_frag : T * Is * 4);
   p.Y = take(small && d * (P + T) > P * d ? d * (P + T) * 4 : P * d * 4);
   p.Ys = take(Is ? T * d * 4 : 0);
   p.Xperm = take(tc_shape_ok(c) ? P * d * 2 : 0);
+  p.Gs = take(small ? kDecodeKSplit * 2 * T * Is * 4 : 0);
   p.total = off;
   return p;
 }
@@ -616,6 +626,7 @@ moe_status_t enqueue_fused(const void* x, const float* r_attn, const void* W_rou
   a.H = at<float>(c, p.H);
   a.Hs = at<float>(c, p.Hs);
   a.Yg = at<float>(c, p.Y);
+  a.Gs = at<float>(c, p.Gs);
   a.ctrl = at<Ctrl>(c, 0);
   a.T = c->T; a.d = c->d_model; a.E = c->n_experts; a.k = c->top_k;
   a.I = c->d_ff; a.Is = c->d_ff_shared;

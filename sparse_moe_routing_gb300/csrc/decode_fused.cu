@@ -114,6 +114,12 @@ __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, uint64_
       "l"(reinterpret_cast<uint64_t>(map)), "r"(su32(bar)), "r"(x), "r"(y)
       : "memory");
 }
+__device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long long* p,
+                                                                   unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -223,9 +229,10 @@ __device__ bool grid_barrier(const Block& B, bool arrive) {
   if (threadIdx.x == 0) {
     bool ok = arrive && !*B.abort_flag;
     if (ok) {
-      __threadfence();
+      // release: the block's writes before the __syncthreads above are
+      // ordered before the arrival; the polls below acquire the others'
       const unsigned long long nb = gridDim.x;
-      const unsigned long long prev = atomicAdd(&B.ctrl->grid_arrivals, 1ull);
+      const unsigned long long prev = atom_add_release_u64(&B.ctrl->grid_arrivals, 1ull);
       const unsigned long long target = (prev / nb + 1) * nb;
       if (prev + 1 != target) {
         const uint64_t t0 = globaltimer_ns();
@@ -238,7 +245,6 @@ __device__ bool grid_barrier(const Block& B, bool arrive) {
           }
         }
       }
-      __threadfence();
     }
     *B.bar_flag = ok ? 1 : 0;
   }
@@ -750,10 +756,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Ws_gate/Ws_up, h rows = tokens). Warp w streams the 64-wide K segments
   // w, w + 16, ... of the item's rows; the 16 partial sums meet in shared
   // memory and are added in warp order, then SwiGLU gives bf16 h.
-  auto gateup_items_mma = [&](int lo, int hi, bool sh) {
+  auto gateup_items_mma = [&](int lo, int hi, bool sh, int KS) {
     const int R = sh ? Is : I;
     const int nrb = R / 16;
-    const int per = d / 64 / kWarps;  // K segments per warp and item
+    const int per = d / 64 / kWarps / KS;  // K segments per warp and item
     const CUtensorMap* mgp = sh ? &msg : &mg;
     const CUtensorMap* mup = sh ? &msu : &mu;
     int fit = lo, fj = 0;
@@ -761,12 +767,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto refill = [&]() {
       if (fit >= hi || *B.abort_flag) return;
       if (lane == 0) {
-        const int c = fit / nrb, rb = fit - c * nrb;
+        const int base = fit / KS, ks = fit - base * KS;
+        const int c = base / nrb, rb = base - c * nrb;
         const int y = (sh ? 0 : s_cexp[c] * I) + rb * 16;
         const int st = stage_of(B, warp, jn);
         bar_expect(&B.full[st], 4096u);
         uint8_t* dst = B.ring + (size_t)st * kSB;
-        const int k0 = (warp + kWarps * fj) * 64;
+        const int k0 = (warp + kWarps * (ks * per + fj)) * 64;
         tma2d(dst, mgp, &B.full[st], k0, y);
         tma2d(dst + 2048, mup, &B.full[st], k0, y);
       }
@@ -784,7 +791,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t xf0[8], xf1[8];
     int xc = -1;
     for (int it = lo; it < hi; ++it) {
-      const int c = it / nrb, rb = it - c * nrb;
+      const int base = it / KS, ks = it - base * KS;
+      const int c = base / nrb, rb = base - c * nrb;
       int nj, cs = 0;
       if (sh) {
         nj = min(kNT, T - c * kNT);
@@ -794,12 +802,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool valid = g < nj;
       const int tok = sh ? c * kNT + (valid ? g : 0) : s_gpair[cs + (valid ? g : 0)] / k;
-      if (per <= 2 && c != xc) {
+      const int s0 = ks * per;  // first K segment of the item
+      if (per <= 2 && c * KS + ks != xc) {
         // the chunk's token fragments for this warp's segments, kept while
         // the chunk lasts and loaded before its first tile lands
-        dmma::x_frags(xb, d, tok, valid, warp * 64, lane, xf0);
-        if (per == 2) dmma::x_frags(xb, d, tok, valid, (warp + kWarps) * 64, lane, xf1);
-        xc = c;
+        dmma::x_frags(xb, d, tok, valid, (warp + kWarps * s0) * 64, lane, xf0);
+        if (per == 2) dmma::x_frags(xb, d, tok, valid, (warp + kWarps * (s0 + 1)) * 64, lane, xf1);
+        xc = c * KS + ks;
       }
       float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
       for (int j = 0; j < per; ++j) {
@@ -808,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) f[e] = j ? xf1[e] : xf0[e];
         } else {
-          dmma::x_frags(xb, d, tok, valid, (warp + kWarps * j) * 64, lane, f);
+          dmma::x_frags(xb, d, tok, valid, (warp + kWarps * (s0 + j)) * 64, lane, f);
         }
         const uint8_t* st = acquire(B, warp, jr, lane);
         if (!st) break;
@@ -832,8 +841,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           gs += part[w * 256 + r * 8 + q];
           us += part[w * 256 + 128 + r * 8 + q];
         }
-        // h in fragment order for the down items: chunk c, slot q, k = 16 rb + r
-        if (q < nj) out[dmma::frag_index(c, R, q, rb * 16 + r)] = __float2bfloat16_rn(siluf_(gs) * us);
+        if (q < nj) {
+          if (KS == 1) {
+            // h in fragment order for the down items: chunk c, slot q, k = 16 rb + r
+            out[dmma::frag_index(c, R, q, rb * 16 + r)] = __float2bfloat16_rn(siluf_(gs) * us);
+          } else {
+            // (shared expert only) partial sums of part ks, [ks][gate/up][t][row]
+            const size_t o = ((size_t)ks * 2 * T + c * kNT + q) * Is + rb * 16 + r;
+            a.Gs[o] = gs;
+            a.Gs[o + (size_t)T * Is] = us;
+          }
+        }
       }
       __syncthreads();
     }
@@ -841,17 +859,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Tensor-core router contraction (bf16), block-wide: item = (token chunk,
   // tile of 16 router rows; rows past E read as zeros); the K split and the
   // warp-ordered sum are those of gateup_items_mma.
-  auto router_items_mma = [&](int lo, int hi, int ntiles) {
-    const int per = d / 64 / kWarps;
+  auto router_items_mma = [&](int lo, int hi, int ntiles, int KS) {
+    const int per = d / 64 / kWarps / KS;  // K segments per warp and item
     int fit = lo, fj = 0;
     uint32_t jn = jr;
     auto refill = [&]() {
       if (fit >= hi || *B.abort_flag) return;
       if (lane == 0) {
-        const int tile = fit % ntiles;
+        const int base = fit / KS, ks = fit - base * KS;
+        const int tile = base % ntiles;
         const int st = stage_of(B, warp, jn);
         bar_expect(&B.full[st], 2048u);
-        tma2d(B.ring + (size_t)st * kSB, &mr, &B.full[st], (warp + kWarps * fj) * 64, tile * 16);
+        tma2d(B.ring + (size_t)st * kSB, &mr, &B.full[st], (warp + kWarps * (ks * per + fj)) * 64,
+              tile * 16);
       }
       ++jn;
       if (++fj == per) {
@@ -866,14 +886,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t xf0[8], xf1[8];
     int xc = -1;
     for (int it = lo; it < hi; ++it) {
-      const int c = it / ntiles, tile = it - c * ntiles;
+      const int base = it / KS, ks = it - base * KS;
+      const int c = base / ntiles, tile = base - c * ntiles;
       const int nj = min(kNT, T - c * kNT);
       const bool valid = g < nj;
       const int tok = c * kNT + (valid ? g : 0);
-      if (per <= 2 && c != xc) {
-        dmma::x_frags(xb, d, tok, valid, warp * 64, lane, xf0);
-        if (per == 2) dmma::x_frags(xb, d, tok, valid, (warp + kWarps) * 64, lane, xf1);
-        xc = c;
+      const int s0 = ks * per;  // first K segment of the item
+      if (per <= 2 && c * KS + ks != xc) {
+        dmma::x_frags(xb, d, tok, valid, (warp + kWarps * s0) * 64, lane, xf0);
+        if (per == 2) dmma::x_frags(xb, d, tok, valid, (warp + kWarps * (s0 + 1)) * 64, lane, xf1);
+        xc = c * KS + ks;
       }
       float dr[4] = {0.f, 0.f, 0.f, 0.f};
       for (int j = 0; j < per; ++j) {
@@ -882,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) f[e] = j ? xf1[e] : xf0[e];
         } else {
-          dmma::x_frags(xb, d, tok, valid, (warp + kWarps * j) * 64, lane, f);
+          dmma::x_frags(xb, d, tok, valid, (warp + kWarps * (s0 + j)) * 64, lane, f);
         }
         const uint8_t* st = acquire(B, warp, jr, lane);
         if (!st) break;
@@ -901,7 +923,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q < nj && col < E) {
           float z = 0.f;
           for (int w = 0; w < kWarps; ++w) z += part[w * 256 + r * 8 + q];
-          a.logits[(size_t)(c * kNT + q) * (E + 1) + col] = z;
+          // (a K split's parts go to consecutive [T][E+1] planes)
+          a.logits[(size_t)ks * T * (E + 1) + (size_t)(c * kNT + q) * (E + 1) + col] = z;
         }
       }
       __syncthreads();
@@ -917,6 +940,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
   STAMP(0);
 
+  // Tensor-core variant: phase 1's contractions are split in ks1 parts along
+  // K when the unsplit items would leave more than half of the grid idle
+  // (partial sums: router logits in ks1 planes added by the routing rule,
+  // shared gate/up in Gs, turned into h in phase 2). It depends on the
+  // shape only, so that a routing-only call splits as the layer does.
+  static_assert(kDecodeKSplit == 2, "the routing rule adds at most two partial logits");
+  int ks1 = 1;
+  if constexpr (MMA) {
+    const int nte = route ? (E + 15) / 16 : 0;
+    const int nc = (T + kNT - 1) / kNT;
+    const int n1 = nc * nte + (Is > 0 ? nc * (Is / 16) : 0);
+    if ((d / 64 / kWarps) % kDecodeKSplit == 0 && n1 * kDecodeKSplit <= nb) ks1 = kDecodeKSplit;
+  }
+
+  // shared h from the K parts of phase 1 (this block's share of the T x Is
+  // values, in fragment order for the down items), in phase 2 by warps that
+  // route no token, or by all threads once routing is done
+  auto shared_h = [&](int tid, int nthr) {
+    const int n = T * Is;
+    const int lo = (int)((long long)blockIdx.x * n / nb), hi = (int)((long long)(blockIdx.x + 1) * n / nb);
+    __nv_bfloat16* hs = reinterpret_cast<__nv_bfloat16*>(a.Hs);
+    for (int i = lo + tid; i < hi; i += nthr) {
+      const int t = i / Is, r = i - t * Is;
+      float gs = __ldcg(a.Gs + i), us = __ldcg(a.Gs + (size_t)T * Is + i);
+      for (int q = 1; q < ks1; ++q) {
+        gs += __ldcg(a.Gs + (size_t)q * 2 * T * Is + i);
+        us += __ldcg(a.Gs + (size_t)(q * 2 + 1) * T * Is + i);
+      }
+      hs[dmma::frag_index(t / kNT, Is, t % kNT, r)] = __float2bfloat16_rn(siluf_(gs) * us);
+    }
+  };
+  const bool split_h = MMA && shared && ks1 > 1;
   // ------------------------------------------------------------- phase 1
   // logit items (token chunk, row): router rows 0..E-1 (route mode), then the
   // shared-gate row E when the gate is not given; then shared gate/up items
@@ -1009,10 +1064,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if constexpr (MMA) {
       // one list of block-wide items, router tiles of 16 experts first, then
-      // the shared expert's 16-row blocks, cut evenly over the blocks
+      // the shared expert's 16-row blocks, each cut into ks1 K parts, cut
+      // evenly over the blocks
       const int nte = route ? (E + 15) / 16 : 0;
-      const int nR = ((T + kNT - 1) / kNT) * nte;
-      const int nSh = shared ? nsh * (Is / 16) : 0;
+      const int nR = ((T + kNT - 1) / kNT) * nte * ks1;
+      const int nSh = shared ? nsh * (Is / 16) * ks1 : 0;
       int blo, bhi;
       block_range(nR + nSh, blo, bhi);
       // the shared-gate row: K split over all threads of one block with no
@@ -1065,9 +1121,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         STAMP(10);
       }
-      router_items_mma(min(blo, nR), min(bhi, nR), nte);
+      router_items_mma(min(blo, nR), min(bhi, nR), nte, ks1);
       if (blo < nR) STAMP(8);
-      if (shared) gateup_items_mma(max(blo, nR) - nR, max(bhi, nR) - nR, true);
+      if (shared) gateup_items_mma(max(blo, nR) - nR, max(bhi, nR) - nR, true, ks1);
       if (shared && bhi > nR) STAMP(9);
     }
   }
@@ -1076,6 +1132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   STAMP(2);
 
   // ------------------------------------------------------------- phase 2
+  if (split_h && T < kWarps && warp >= T) shared_h(threadIdx.x - T * 32, kThreads - T * 32);
   if (route) {
     if (warp < T) {
       TopkArgs ta{};
@@ -1093,6 +1150,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ta.has_shared_logit = sgate ? 1 : 0;
       ta.routed_scaling = a.routed_scaling;
       ta.renorm_clamp = a.renorm_clamp;
+      ta.nparts = ks1;
+      ta.part_stride = (size_t)T * (E + 1);
       topk_token_pl<PL>(ta, warp, lane);
     }
   } else {
@@ -1107,6 +1166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  if (split_h && T >= kWarps) {
+    shared_h(threadIdx.x, kThreads);
+    __syncthreads();
+  }
   STAMP(3);
   if (sh_early && warp >= T) {
     const int nsh = (T + kNT - 1) / kNT;
@@ -1129,14 +1192,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_key[p] = ok ? e : E;
   }
   __syncthreads();
-  for (int p = threadIdx.x; p < P; p += kThreads) {
-    const int key = s_key[p];
+  {
+    // rank of pair p: G consecutive threads count over every G-th pair and
+    // add their counts with shuffles (G a power of two, G P <= threads)
+    int G = 16;
+    while (G > 1 && G * P > kThreads) G >>= 1;
+    const int p = threadIdx.x / G, sub = threadIdx.x & (G - 1);
+    const int key = p < P ? s_key[p] : 0;
     int rank = 0;
-    for (int q = 0; q < P; ++q) {
-      const int kq = s_key[q];
-      rank += (kq < key || (kq == key && q < p)) ? 1 : 0;
-    }
-    s_gpair[rank] = p;
+    if (p < P)
+      for (int q = sub; q < P; q += G) {
+        const int kq = s_key[q];
+        rank += (kq < key || (kq == key && q < p)) ? 1 : 0;
+      }
+    for (int o = G >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (p < P && sub == 0) s_gpair[rank] = p;
   }
   __syncthreads();
   // chunks: runs of one expert in the sorted order, cut every kNT pairs
@@ -1196,7 +1266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int lo, hi;
     if constexpr (MMA) {
       block_range(nch * (I / 16), lo, hi);
-      gateup_items_mma(lo, hi, false);
+      gateup_items_mma(lo, hi, false, 1);
       lo = hi = 0;  // the per-warp rows below have no work
     } else {
       block_range(nch * I, lo, hi);
@@ -1354,6 +1424,8 @@ bool decode_fused_supported(int T, int d, int E, int k, int I, int Is, int act, 
   const bool mma = mma_shape(d, I, Is, act == MOE_BF16);
   return ring_stages(T, k, max_cols(d, tc_sm_count(), mma ? 8 : 4), mma) > 0;
 }
+
+bool decode_fused_mma(int d, int I, int Is) { return mma_shape(d, I, Is, true); }
 
 cudaError_t launch_decode_fused(const DecodeArgs& a, bool bf16, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;

@@ -28,6 +28,10 @@ struct TopkArgs {
   float* s_shared;        // [T] or null
   int T, E, k, kind, n_group, topk_group, has_shared_logit;
   float routed_scaling, renorm_clamp;
+  // logits of experts held as nparts partial sums (0 or 1: one; at most 2)
+  // at logits + i * part_stride, added in part order; column E in part 0 only
+  int nparts;
+  size_t part_stride;
 };
 
 struct BucketArgs {
@@ -95,10 +99,11 @@ struct DecodeArgs {
   float* out;               // [T][d]
   int32_t* topk_ids;        // route mode outputs [T][k]
   float* weights;
-  float* logits;            // workspace [T][E+1]
+  float* logits;            // workspace [T][E+1] x kDecodeKSplit (partial sums of a K split)
   float* H;                 // workspace [T*k][I] fp32
   float* Hs;                // workspace [T][Is] fp32
   float* Yg;                // workspace [d][T*k + T]: per-column slot results (tensor-core variant)
+  float* Gs;                // workspace [kDecodeKSplit][2][T][Is]: shared gate/up partial sums
   Ctrl* ctrl;
   int T, d, E, k, I, Is;
   int kind, n_group, topk_group;
@@ -109,9 +114,14 @@ struct DecodeArgs {
   float* s_out;             // route only: the shared gate [T], or null
 };
 constexpr int kDecodeMaxTokens = 16;
+// The tensor-core variant splits K of its first-phase contractions over this
+// many blocks when the items would otherwise leave most of the grid idle.
+constexpr int kDecodeKSplit = 2;
 // Shapes the single-launch decode kernel takes (T <= kDecodeMaxTokens,
 // f32 or bf16 weights and activations alike, E <= 512, k <= 32).
 bool decode_fused_supported(int T, int d, int E, int k, int I, int Is, int act, int wdt);
+// Whether bf16 shapes (d, I, Is) take the kernel's tensor-core variant.
+bool decode_fused_mma(int d, int I, int Is);
 cudaError_t launch_decode_fused(const DecodeArgs& a, bool bf16, cudaStream_t st);
 
 struct CombineArgs {

@@ -149,10 +149,19 @@ __device__ __forceinline__ void topk_token_pl(const TopkArgs& a, int t, int lane
 
   float key[PL];   // ranking key per owned expert
   float val[PL];   // softmax: logit; sigmoid: raw score s
+  // every load issued before the first use (partial sums: two parts at most)
+  float z0[PL], z1[PL];
+  const bool two = a.nparts > 1;
+#pragma unroll
+  for (int j = 0; j < PL; ++j) {
+    const int e = lane + 32 * j;
+    z0[j] = e < E ? __ldcg(z + e) : -INFINITY;
+    z1[j] = (two && e < E) ? __ldcg(z + a.part_stride + e) : 0.f;
+  }
 #pragma unroll
   for (int j = 0; j < PL; ++j) {
     int e = lane + 32 * j;
-    float zv = e < E ? __ldcg(z + e) : -INFINITY;
+    const float zv = two ? z0[j] + z1[j] : z0[j];
     if (a.kind == 0) {
       key[j] = e < E ? rank_key(zv) : -INFINITY;
       val[j] = zv;
