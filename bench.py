@@ -606,22 +606,23 @@ def run_ours(args):
         del wl1
         return ms1 / K
 
-    def measure(T, main):
+    def measure(T, main, detail=None):
         """The timed replay (no event nodes inside the graph); for the main
-        workload also the clocks during it and, from one more replay with
-        the dominant kernel bracketed by in-graph events, that kernel's mean
-        duration."""
+        workload (and the sweep's decode points, detail) also the clocks
+        during it and, from one more replay with the dominant kernel
+        bracketed by in-graph events, that kernel's mean duration."""
+        detail = main if detail is None else detail
         wl = Workload(weights, T, _n_copies(shape, T), path)
         tc = _uses_tc(shape, T, path)
         fused = _uses_fused(shape, T, path)
         kern = ("decode_fused" if fused else ("tc_gateup" if tc else "gemv_gateup")) \
-            if main else None
-        sampler = ClockSampler(local) if main else None
+            if detail else None
+        sampler = ClockSampler(local) if detail else None
         ms, launches, _, (t0, t1), extra = time_graph(wl, K, W, None, sampler,
                                                      N_EXTRA_REPLAYS if main else 0)
         if main:
             replay_ms[:] = [ms] + extra
-        durs = time_graph(wl, min(K, 100), 3, kern)[2] if main else []
+        durs = time_graph(wl, min(K, 100), 3, kern)[2] if detail else []
         ids = wl.ids.cpu().numpy().ravel()
         n_act = int(np.unique(ids).size)
         if main:
@@ -703,14 +704,37 @@ def run_ours(args):
         sweep = {}
         for Ts in (1, 8, 64):
             if Ts == T:
-                sweep[str(Ts)] = {"tokens_per_s": T * K / (ms / 1e3), "ms_per_step": ms_step,
-                                  "layer_hbm_frac": config["layer_hbm_frac"]}
+                sweep[str(Ts)] = {"T": T, "us_per_layer": ms_step * 1e3,
+                                  "tokens_per_s": T * K / (ms / 1e3), "ms_per_step": ms_step,
+                                  "expert_path": config["expert_path"],
+                                  "layer_floor_us": floor_us,
+                                  "layer_floor_frac": config["layer_floor_frac"],
+                                  "layer_hbm_frac": config["layer_hbm_frac"],
+                                  "dominant": {k_: roofline[k_] for k_ in
+                                               ("kernel", "bound", "mean_launch_us", "achieved",
+                                                "peak", "unit", "frac")},
+                                  "clocks": clocks}
                 continue
-            wls, mss, _, _, na, _, _ = measure(Ts, False)
-            b = layer_bytes(shape, Ts, na)
-            sweep[str(Ts)] = {"tokens_per_s": Ts * K / (mss / 1e3), "ms_per_step": mss / K,
-                              "active_experts": na,
-                              "layer_hbm_frac": b / (mss / K * 1e-3) / 1e9 / hbm}
+            wls, mss, _, dus, na, cls, kn = measure(Ts, False, True)
+            b, f = layer_bytes(shape, Ts, na), layer_flops(shape, Ts)
+            us = mss / K * 1e3
+            fl = max(b / (hbm * 1e9), f / (tflops * 1e12)) * 1e6
+            if kn == "decode_fused":
+                kb_, kf_ = b, f
+            else:
+                kb_, kf_ = gateup_work(shape, Ts, na)
+            mk = sum(dus) / len(dus) if dus else None
+            kach = kb_ / (mk * 1e-3) / 1e9 if mk else None
+            sweep[str(Ts)] = {"T": Ts, "us_per_layer": us, "tokens_per_s": Ts * K / (mss / 1e3),
+                              "ms_per_step": mss / K, "active_experts": na,
+                              "expert_path": _expert_path(shape, Ts, path),
+                              "layer_floor_us": fl, "layer_floor_frac": fl / us,
+                              "layer_hbm_frac": b / (mss / K * 1e-3) / 1e9 / hbm,
+                              "dominant": {"kernel": kn, "bound": "hbm",
+                                           "mean_launch_us": mk * 1e3 if mk else None,
+                                           "achieved": kach, "peak": hbm, "unit": "GB/s",
+                                           "frac": kach / hbm if kach else None},
+                              "clocks": cls}
             del wls
             if not args.no_hot_l2:
                 sweep[str(Ts)]["hot_l2_ms_per_step"] = hot_l2(Ts)
