@@ -1,5 +1,5 @@
 // Persistent grouped GEMM on the fifth-generation tensor cores (sm_103a):
-// TMA tile loads (128-byte swizzle) feed a 4-stage mbarrier pipeline, one
+// TMA tile loads (128-byte swizzle) feed a multi-stage mbarrier pipeline, one
 // elected thread issues tcgen05.mma (bf16 x bf16 -> fp32) into a
 // double-buffered TMEM accumulator, and four epilogue warps drain TMEM with
 // tcgen05.ld and apply the fused epilogue while the next tile accumulates.
@@ -30,7 +30,8 @@ namespace moe {
 namespace {
 
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 2-5
-// epilogue, and (4-bit weights only) warps 6-13 dequantise the B stages.
+// epilogue, and (4-bit weights only) warps 6-13 dequantise the B stages and
+// warp 14 brings their raw codes.
 constexpr int BM = 128, BK = 64;
 constexpr uint32_t kTmemCols = 512;
 
@@ -207,15 +208,19 @@ constexpr int kEpiRowBytes = 144;
 constexpr int kEpiWarpBytes = 32 * kEpiRowBytes;
 
 // 4-bit weights: warps 6 .. 6 + kDequantWarps - 1 dequantise the B stages,
-// one B row (of 256) per thread.
+// one B row (of 256) per thread; warp 6 + kDequantWarps brings the raw codes.
 constexpr int kDequantWarps = 8;
+constexpr int kRowThreads = kDequantWarps / 8;  // threads per B row (256 rows per stage)
 
 // Shared-memory plan of one CTA (1024-byte aligned stages). bf16: kStages
-// stages of A + B. 4-bit: kStages stages of A + raw codes (filled by TMA,
-// freed by the MMA) and kBStages dequantised B stages (filled by the
-// dequant warps, freed by the MMA), so the copies run further ahead than
-// 48 KB stages would allow. EPI: the down epilogue's staging rows (the other
-// modes leave that shared memory to the pipeline).
+// stages of A + B, filled by one TMA producer and freed by the MMA. 4-bit:
+// three rings. kStages A stages (TMA, freed by the MMA); kCStages raw-code
+// stages (TMA from a second producer warp, freed by the dequant warps once
+// they have read them); kBStages dequantised B stages (filled by the dequant
+// warps, freed by the MMA). The code ring runs furthest ahead, so that the
+// dequantisation of a stage never waits for its codes to cross DRAM; the A
+// ring only has to land before the MMA reaches it. EPI: the down epilogue's
+// staging rows (the other modes leave that shared memory to the pipeline).
 //
 // RB = row blocks per work item. RB = 2 ("paired" items, used for 4-bit
 // banks): two 128-row blocks of one group share each B stage (two A tiles
@@ -237,26 +242,34 @@ struct SmemPlan {
   static_assert(AR == 128 || ((AR == 64 || AR == 16) && !Q4 && RB == 1), "short A: bf16, unpaired");
   static constexpr int kStageA = AR * BK * 2;  // bytes of one A stage
   static constexpr int kStageB = NB * BK * 2;  // bytes of one B stage
-  static constexpr size_t kEpiBytes = EPI ? 4 * (size_t)kEpiWarpBytes : 0;
-  static constexpr int kFit = (int)((227 * 1024 - 2048 - kEpiBytes) / (kStageA + kStageB));
-  static constexpr bool kNarrow = !Q4 && RB == 1 && (NB < 256 || AR < 128);
-  static constexpr int kStages =
-      kNarrow ? (kFit > 12 ? 12 : kFit) : (RB == 2 ? (EPI ? 3 : 4) : (Q4 ? 5 : 4));
-  static constexpr int kBStages = Q4 ? 2 : kStages;
-  static constexpr int kNAcc = 2 / RB;   // accumulator buffers of RB x 256 TMEM columns
   static constexpr int kStageQ = 256 * (BK / 2);  // raw 4-bit codes of one B stage
-  static constexpr int kThreadsCta = Q4 ? 192 + 32 * kDequantWarps : 192;
+  static constexpr size_t kEpiBytes = EPI ? 4 * (size_t)kEpiWarpBytes : 0;
+  static constexpr size_t kAvail = 227 * 1024 - 2048 - kEpiBytes;
+  static constexpr int kFit = (int)(kAvail / (kStageA + kStageB));
+  static constexpr bool kNarrow = !Q4 && RB == 1 && (NB < 256 || AR < 128);
+  static constexpr int kBStages = Q4 ? ((EPI && RB == 2) ? 2 : 3) : 0;
+  static constexpr int kCStages = Q4 ? 4 : 0;
+  static constexpr int kQ4Fit =
+      (int)((kAvail - (size_t)kBStages * kStageB - (size_t)kCStages * kStageQ) /
+            ((size_t)RB * kStageA));
+  static constexpr int kStages =
+      Q4 ? (kQ4Fit > 5 ? 5 : kQ4Fit)
+         : (kNarrow ? (kFit > 12 ? 12 : kFit) : (RB == 2 ? (EPI ? 3 : 4) : 4));
+  static constexpr int kNAcc = 2 / RB;   // accumulator buffers of RB x 256 TMEM columns
+  static constexpr int kThreadsCta = Q4 ? 192 + 32 * kDequantWarps + 32 : 192;
   static constexpr size_t kA = 0;
   static constexpr size_t kB = kA + (size_t)kStages * RB * kStageA;
-  static constexpr size_t kQ = kB + (size_t)kBStages * kStageB;
-  static constexpr size_t kEpi = kQ + (Q4 ? (size_t)kStages * kStageQ : 0);
+  static constexpr size_t kQ = kB + (size_t)(Q4 ? kBStages : kStages) * kStageB;
+  static constexpr size_t kEpi = kQ + (size_t)kCStages * kStageQ;
   static constexpr size_t kBars = kEpi + kEpiBytes;
-  // full, empty, rawfull per stage; bfull, bempty per B stage; tfull and
-  // tempty per accumulator (two slots each); then the TMEM address word and
-  // the abort flag
-  static constexpr size_t kBarBytes = ((3 * kStages + 2 * kBStages + 4) * 8 + 8 + 127) / 128 * 128;
+  // full and empty per A (+ B for bf16) stage; rawfull and rawempty per code
+  // stage; bfull and bempty per B stage; tfull and tempty per accumulator
+  // (two slots each); then the TMEM address word and the abort flag
+  static constexpr size_t kBarBytes =
+      ((2 * kStages + 2 * kCStages + 2 * kBStages + 4) * 8 + 8 + 127) / 128 * 128;
   static constexpr size_t kBytes = 1024 + kBars + kBarBytes;
   static_assert(kBytes <= 227 * 1024, "shared memory plan exceeds 227 KB");
+  static_assert(!Q4 || kStages >= 3, "4-bit plan: at least three A stages");
 };
 
 // The (scale, min) arrays of the B row a dequant thread owns: bank row and
@@ -295,15 +308,25 @@ __device__ __forceinline__ uint32_t bf16_at(const uint4& v, int j) {
 // e), 128 is subtracted exactly, and one fused multiply-add rounds
 // scale * q + min once.
 __device__ __forceinline__ void dequant_row(const uint8_t* q_row_src, uint8_t* b_stage, int r,
-                                            uint32_t scale_bits, uint32_t min_bits) {
+                                            int part, uint32_t scale_bits, uint32_t min_bits) {
   const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)scale_bits),
                                                 __ushort_as_bfloat16((unsigned short)scale_bits));
   const __nv_bfloat162 m2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)min_bits),
                                                 __ushort_as_bfloat16((unsigned short)min_bits));
   const __nv_bfloat162 b128 = __float2bfloat162_rn(128.0f);
-  const uint4 c0 = reinterpret_cast<const uint4*>(q_row_src)[0];
-  const uint4 c1 = reinterpret_cast<const uint4*>(q_row_src)[1];
-  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  // this thread's share of the row: words [c0w, c0w + kW) (16 B of codes per
+  // 32 weights)
+  constexpr int kW = 8 / kRowThreads;
+  const int c0w = part * kW;
+  uint32_t words[kW];
+#pragma unroll
+  for (int h = 0; h < kW / 4; ++h) {
+    const uint4 c = reinterpret_cast<const uint4*>(q_row_src)[c0w / 4 + h];
+    words[4 * h] = c.x;
+    words[4 * h + 1] = c.y;
+    words[4 * h + 2] = c.z;
+    words[4 * h + 3] = c.w;
+  }
   uint8_t* row_base = b_stage + (r >> 3) * 1024 + (r & 7) * 128;
   auto deq = [&](uint32_t pair_bits) {  // (128 + e_lo, 128 + e_hi) -> (w_lo, w_hi)
     __nv_bfloat162 q = *reinterpret_cast<__nv_bfloat162*>(&pair_bits);
@@ -311,10 +334,11 @@ __device__ __forceinline__ void dequant_row(const uint8_t* q_row_src, uint8_t* b
     return *reinterpret_cast<const uint32_t*>(&w);
   };
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int cw = 0; cw < kW; ++cw) {
     // word c holds elements 8c..8c+7, the even element in the low nibble:
     // element e at bits 4e..4e+3
-    const uint32_t x = words[c];
+    const int c = c0w + cw;
+    const uint32_t x = words[cw];
     const uint32_t h04 = deq((x & 0x000F000Fu) | 0x43004300u);          // e0, e4
     const uint32_t h15 = deq(((x >> 4) & 0x000F000Fu) | 0x43004300u);   // e1, e5
     const uint32_t h26 = deq(((x >> 8) & 0x000F000Fu) | 0x43004300u);   // e2, e6
@@ -343,11 +367,12 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
   uint8_t* sB = smem + SP::kB;
   uint8_t* sQ = smem + SP::kQ;
   uint8_t* sEpi = smem + SP::kEpi;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SP::kBars);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SP::kBars);  // A (+ B for bf16) landed
   uint64_t* empty = full + STAGES;
-  uint64_t* rawfull = empty + STAGES;   // Q4 only: A tile + raw codes landed
-  uint64_t* bfull = rawfull + STAGES;   // Q4 only: B stage dequantised
-  uint64_t* bempty = bfull + SP::kBStages;  // Q4 only: B stage consumed
+  uint64_t* rawfull = empty + STAGES;           // Q4 only: raw codes landed
+  uint64_t* rawempty = rawfull + SP::kCStages;  // Q4 only: codes read by every dequant warp
+  uint64_t* bfull = rawempty + SP::kCStages;    // Q4 only: B stage dequantised
+  uint64_t* bempty = bfull + SP::kBStages;      // Q4 only: B stage consumed
   uint64_t* tfull = bempty + SP::kBStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
@@ -359,7 +384,10 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < SP::kCStages; ++s) {
       mbar_init(&rawfull[s], 1);
+      mbar_init(&rawempty[s], kDequantWarps);  // one arrival per dequant warp
     }
     for (int s = 0; s < SP::kBStages; ++s) {
       mbar_init(&bfull[s], kDequantWarps);  // one arrival per dequant warp
@@ -395,10 +423,9 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
   // MMAs. A wait's outcome is lane 0's, broadcast to the warp.
   if (warp == 0) {
     // -------------------------------------------------------------- producer
-    // bf16 B: A + B tiles land on full[]. Q4 B: A + raw code tiles land on
-    // rawfull[] and the dequant warps then fill a stage of the B ring.
-    const uint32_t stage_bytes =
-        Q4 ? kStageA + a.bn * (BK / 2) : kStageA + a.bn * BK * 2;
+    // A tiles (+ bf16 B tiles) land on full[]; 4-bit codes come from their
+    // own producer warp.
+    const uint32_t stage_bytes = Q4 ? kStageA : kStageA + a.bn * BK * 2;
     int stage = 0;
     uint32_t ph = 0;
     bool alive = true;
@@ -422,16 +449,11 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
           break;
         }
         if (lane == 0) {
-          uint64_t* bar = Q4 ? &rawfull[stage] : &full[stage];
+          uint64_t* bar = &full[stage];
           mbar_expect_tx(bar, item_bytes);
           tma_load_2d(sA + stage * RB * kStageA, mA, bar, kb * BK, arow);
           if (two) tma_load_2d(sA + (stage * RB + 1) * kStageA, mA, bar, kb * BK, arow + BM);
-          if (Q4) {
-            uint8_t* q_dst = sQ + stage * SP::kStageQ;
-            tma_load_2d(q_dst, mB0, bar, kb * (BK / 2), brow);
-            if (MODE == kTcGateUp)
-              tma_load_2d(q_dst + bhalf * (BK / 2), mB1, bar, kb * (BK / 2), brow);
-          } else {
+          if (!Q4) {
             uint8_t* b_dst = sB + stage * kStageB;
             tma_load_2d(b_dst, mB0, bar, kb * BK, brow);
             if (MODE == kTcGateUp)
@@ -478,12 +500,8 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
       for (int kb = 0; kb < nkb; ++kb) {
         ok = true;
         if (lane == 0) {
-          if (Q4) {
-            ok = mbar_wait(&rawfull[stage], ph, lim);     // the A tile of this stage
-            if (ok) ok = mbar_wait(&bfull[bs], bph, lim);  // its dequantised B stage
-          } else {
-            ok = mbar_wait(&full[stage], ph, lim);
-          }
+          ok = mbar_wait(&full[stage], ph, lim);             // the A (+ bf16 B) tiles
+          if (Q4 && ok) ok = mbar_wait(&bfull[bs], bph, lim);  // the dequantised B stage
         }
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
         if (!ok) {
@@ -628,18 +646,56 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
         aph ^= 1u;
       }
     }
+  } else if (Q4 && warp >= 6 + kDequantWarps) {
+    // ------------------------------------------------------- code producer
+    // Raw 4-bit codes of each (tile, k-block) into the code ring, as soon as
+    // every dequant warp has read the stage's previous contents.
+    int cs = 0;
+    uint32_t cph = 0;
+    bool alive = true;
+    const uint32_t code_bytes = a.bn * (BK / 2);
+    for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
+      const TileInfo ti = decode_tile<MODE>(a, t, n_rb);
+      const CUtensorMap* mB0 = ti.shared ? &tmB2 : &tmB0;
+      const CUtensorMap* mB1 = ti.shared ? &tmB3 : &tmB1;
+      const int bhalf = MODE == kTcGateUp ? a.bn / 2 : a.bn;
+      const int brow = (ti.shared ? 0 : ti.g * a.brows_routed) + ti.nt * bhalf;
+      for (int kb = 0; kb < nkb; ++kb) {
+        bool ok = lane == 0 ? mbar_wait(&rawempty[cs], cph ^ 1u, lim) : true;
+        ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
+        if (!ok) {
+          if (lane == 0) give_up(a, abort_flag, site);
+          alive = false;
+          break;
+        }
+        if (lane == 0) {
+          uint64_t* bar = &rawfull[cs];
+          mbar_expect_tx(bar, code_bytes);
+          uint8_t* q_dst = sQ + cs * SP::kStageQ;
+          tma_load_2d(q_dst, mB0, bar, kb * (BK / 2), brow);
+          if (MODE == kTcGateUp) tma_load_2d(q_dst + bhalf * (BK / 2), mB1, bar, kb * (BK / 2), brow);
+        }
+        __syncwarp();
+        if (++cs == SP::kCStages) {
+          cs = 0;
+          cph ^= 1u;
+        }
+      }
+    }
   } else if (Q4) {
     // --------------------------------------------------------------- dequant
-    // The dequant warps follow the producer's (tile, k-block) order: wait for
-    // the raw stage, write the bf16 B stage, make the generic-proxy writes
-    // visible to the tensor core's async proxy, then arrive on full[] (one
-    // arrival per warp). Thread r owns B row r. When a row's group count is a
-    // multiple of 8, its scales and mins are read 8 groups (16 B) at a time,
-    // one block of 8 k-blocks ahead of use.
-    const int r = threadIdx.x - 192;
+    // The dequant warps follow the producers' (tile, k-block) order: wait for
+    // the code stage and a free B stage, write the bf16 B stage, make the
+    // generic-proxy writes visible to the tensor core's async proxy, then
+    // arrive on bfull[] and rawempty[] (one arrival per warp each). Thread r
+    // owns B row r. When a row's group count is a multiple of 8, its scales
+    // and mins are read 8 groups (16 B) at a time, one block of 8 k-blocks
+    // ahead of use.
+    const int r = (threadIdx.x - 192) / kRowThreads;     // B row of this thread
+    const int part = (threadIdx.x - 192) % kRowThreads;  // its share of the row
     const bool vec = (a.qgroups & 7) == 0;
-    int stage = 0, bs = 0;
-    uint32_t ph = 0, bph = 0;
+    int cs = 0, bs = 0;
+    uint32_t cph = 0, bph = 0;
     bool alive = true;
     for (int t = blockIdx.x; t < total && alive; t += gridDim.x) {
       const TileInfo ti = decode_tile<MODE>(a, t, n_rb);
@@ -671,7 +727,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
         }
         bool ok = true;
         if (lane == 0) {
-          ok = mbar_wait(&rawfull[stage], ph, lim);
+          ok = mbar_wait(&rawfull[cs], cph, lim);
           if (ok) ok = mbar_wait(&bempty[bs], bph ^ 1u, lim);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
@@ -680,13 +736,16 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
           alive = false;
           break;
         }
-        dequant_row(sQ + stage * SP::kStageQ + r * 32, sB + bs * kStageB, r, sbits, mbits);
+        dequant_row(sQ + cs * SP::kStageQ + r * 32, sB + bs * kStageB, r, part, sbits, mbits);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bfull[bs]);
-        if (++stage == STAGES) {
-          stage = 0;
-          ph ^= 1u;
+        if (lane == 0) {
+          mbar_arrive(&bfull[bs]);
+          mbar_arrive(&rawempty[cs]);
+        }
+        if (++cs == SP::kCStages) {
+          cs = 0;
+          cph ^= 1u;
         }
         if (++bs == SP::kBStages) {
           bs = 0;
