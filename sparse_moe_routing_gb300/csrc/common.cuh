@@ -95,7 +95,12 @@ __device__ __forceinline__ void store_act(__nv_bfloat16* p, size_t i, float v) {
 }
 
 __device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + __expf(-v)); }
-__device__ __forceinline__ float siluf_(float v) { return v / (1.0f + __expf(-v)); }
+// SiLU with the fast division (reciprocal + multiply, 2 ulp): its result
+// is rounded to bf16 or summed in fp32 right after, and the IEEE division
+// made the tensor-core epilogues that apply it the slowest stage of the
+// 4-bit gate/up kernel (1055 -> 891 us at the Mixtral shape). As v -> -inf
+// the denominator overflows to inf and the quotient is 0, SiLU's limit.
+__device__ __forceinline__ float siluf_(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // Programmatic dependent launch: every kernel is launched so that it may be
 // scheduled while its predecessor on the stream finishes. pdl_wait() blocks
