@@ -587,6 +587,16 @@ moe_status_t enqueue_experts(const void* x, const float* r_attn, const int32_t* 
     return small ? launch_gemv_small(g, act, wdt, false, st) : launch_gemv_gateup(g, act, wdt, st);
   });
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  g.r_attn = r_attn;
+  g.out = out;
+  if (small && gemv_small_down_combine_ok(g)) {
+    // one kernel for down and combine (a token's few pairs and its shared
+    // expert fit one CTA per output column group): one launch fewer on the
+    // latency-bound single-token path
+    return cuda_status(run(MOE_KERNEL_GEMV_DOWN, st, [&] {
+      return launch_gemv_small_down_combine(g, act, wdt, st);
+    }));
+  }
   e = run(MOE_KERNEL_GEMV_DOWN, st, [&] {
     return small ? launch_gemv_small(g, act, wdt, true, st) : launch_gemv_down(g, act, wdt, st);
   });

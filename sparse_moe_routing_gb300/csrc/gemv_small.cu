@@ -142,12 +142,13 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_small_gateup(GemvArgs a) {
     gateup_rows<TW, NT>(a, v, row, wg, wu, j0, min(NT, v.n - j0), lane);
 }
 
-// Y[i][col] = scale_i * (W_down[col] . h_i) for kDnRows consecutive columns
-// col0.. and the group's tokens i in [j0, j0 + nj); scale = the routing
-// weight (routed) or the shared gate; one whole warp.
-template <typename TW, int NT>
-__device__ __forceinline__ void down_rows(const GemvArgs& a, const SGroup& v, int col0, int nr,
-                                          const TW* Wd, const TW* Hb, int j0, int nj, int lane) {
+// scale_i * (W_down[col] . h_i) for kDnRows consecutive columns col0.. and
+// the group's tokens i in [j0, j0 + nj); scale = the routing weight (routed)
+// or the shared gate; one whole warp. put(r, i, value) stores each result
+// (called by one lane per (column, token)).
+template <typename TW, int NT, typename Put>
+__device__ __forceinline__ void down_dots(const GemvArgs& a, const SGroup& v, int nr, const TW* Wd,
+                                          const TW* Hb, int j0, int nj, int lane, Put put_result) {
   constexpr int kVec = Chunk<TW>::kVec;
   const int K = v.width;
   constexpr int NV = P2<kDnRows * NT>::v;
@@ -185,10 +186,19 @@ __device__ __forceinline__ void down_rows(const GemvArgs& a, const SGroup& v, in
       const int i = j0 + j;
       const float scale = v.shared ? a.s_shared[i]
                                    : a.alpha[a.pair_ids ? v.row0 + i : a.perm[v.row0 + i]];
-      float* Y = v.shared ? a.Ys + (size_t)i * a.d : a.Y + (size_t)(v.row0 + i) * a.d;
-      Y[col0 + r] = scale * sum;
+      put_result(r, i, scale * sum);
     }
   }
+}
+
+// Y[i][col] for the group's tokens (packed rows, or token rows of Ys).
+template <typename TW, int NT>
+__device__ __forceinline__ void down_rows(const GemvArgs& a, const SGroup& v, int col0, int nr,
+                                          const TW* Wd, const TW* Hb, int j0, int nj, int lane) {
+  down_dots<TW, NT>(a, v, nr, Wd, Hb, j0, nj, lane, [&](int r, int i, float y) {
+    float* Y = v.shared ? a.Ys + (size_t)i * a.d : a.Y + (size_t)(v.row0 + i) * a.d;
+    Y[col0 + r] = y;
+  });
 }
 
 template <typename TW, int NT>
@@ -207,6 +217,52 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_small_down(GemvArgs a) {
   const int nr = min(kDnRows, a.d - col0);
   for (int j0 = 0; j0 < v.n; j0 += NT)
     down_rows<TW, NT>(a, v, col0, nr, Wd, Hb, j0, min(NT, v.n - j0), lane);
+}
+
+// Down + combine for pair groups: CTA b owns the kDnRows output columns
+// 4b.. of every token; its warps compute those columns for every (token,
+// slot) pair and for the shared expert (warp w: groups w, w + kWarps, ...),
+// then the CTA adds them as the combine kernel does: out[t] = r_attn[t] +
+// ((sum over slots s, in slot order) + shared). The same products and the
+// same summation order, so the results are those of the two-kernel path.
+constexpr int kDcMaxGroups = 2 * kWarps;
+template <typename TW, int NT>
+__global__ void __launch_bounds__(kWarps * 32) gemv_small_down_combine(GemvArgs a) {
+  __shared__ float sy[kDcMaxGroups][kDnRows];                   // pair p = t * k + s
+  __shared__ float sys[kGemvSmallTokens][kDnRows];             // shared expert, token t
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col0 = blockIdx.x * kDnRows;
+  const int nr = min(kDnRows, a.d - col0);
+  for (int i = threadIdx.x; i < kDcMaxGroups * kDnRows; i += kWarps * 32) (&sy[0][0])[i] = 0.f;
+  for (int i = threadIdx.x; i < kGemvSmallTokens * kDnRows; i += kWarps * 32) (&sys[0][0])[i] = 0.f;
+  __syncthreads();
+  const int G = a.routed_slots + (a.has_shared ? 1 : 0);
+  for (int gi = warp; gi < G; gi += kWarps) {
+    const SGroup v = group_at(a, gi);
+    if (!v.ok) continue;  // a bad id (reported): the pair adds nothing
+    const TW* Wd = static_cast<const TW*>(v.shared ? a.Wsd : a.Wd) +
+                   (v.shared ? 0 : (size_t)v.g * a.d * a.I) + (size_t)col0 * v.width;
+    const TW* Hb = static_cast<const TW*>(v.shared ? a.Hs : a.H) +
+                   (v.shared ? 0 : (size_t)v.row0 * a.I);
+    for (int j0 = 0; j0 < v.n; j0 += NT)
+      down_dots<TW, NT>(a, v, nr, Wd, Hb, j0, min(NT, v.n - j0), lane, [&](int r, int i, float y) {
+        if (v.shared) sys[i][r] = y;
+        else sy[gi][r] = y;
+      });
+  }
+  __syncthreads();
+  if (threadIdx.x < a.T * kDnRows) {
+    const int t = threadIdx.x / kDnRows, r = threadIdx.x - t * kDnRows;
+    if (r < nr) {
+      float acc = 0.f;
+      for (int s = 0; s < a.k; ++s) acc += sy[t * a.k + s][r];
+      if (a.has_shared) acc += sys[t][r];
+      const size_t o = (size_t)t * a.d + col0 + r;
+      a.out[o] = a.r_attn[o] + acc;
+    }
+  }
 }
 
 template <typename TW, int NT>
@@ -234,6 +290,31 @@ cudaError_t dispatch(const GemvArgs& a, bool down, cudaStream_t st) {
 }
 
 }  // namespace
+
+bool gemv_small_down_combine_ok(const GemvArgs& a) {
+  return a.pair_ids != nullptr && a.T >= 1 && a.T <= kGemvSmallTokens &&
+         a.routed_slots + (a.has_shared ? 1 : 0) <= kDcMaxGroups && a.d % kDnRows == 0;
+}
+
+cudaError_t launch_gemv_small_down_combine(const GemvArgs& a, int act, int wdt, cudaStream_t st) {
+  if (!gemv_small_down_combine_ok(a) || a.d % 8 != 0 || a.I % 8 != 0 || a.Is % 8 != 0)
+    return cudaErrorInvalidValue;
+  const dim3 grid(a.d / kDnRows);
+  if (wdt == 0 && act == 0) {
+    if (a.T <= 1) return launch_pdl(gemv_small_down_combine<float, 1>, grid, kWarps * 32, 0, st, a);
+    if (a.T <= 2) return launch_pdl(gemv_small_down_combine<float, 2>, grid, kWarps * 32, 0, st, a);
+    if (a.T <= 4) return launch_pdl(gemv_small_down_combine<float, 4>, grid, kWarps * 32, 0, st, a);
+    return launch_pdl(gemv_small_down_combine<float, 8>, grid, kWarps * 32, 0, st, a);
+  }
+  if (wdt == 1 && act == 1) {
+    using B = __nv_bfloat16;
+    if (a.T <= 1) return launch_pdl(gemv_small_down_combine<B, 1>, grid, kWarps * 32, 0, st, a);
+    if (a.T <= 2) return launch_pdl(gemv_small_down_combine<B, 2>, grid, kWarps * 32, 0, st, a);
+    if (a.T <= 4) return launch_pdl(gemv_small_down_combine<B, 4>, grid, kWarps * 32, 0, st, a);
+    return launch_pdl(gemv_small_down_combine<B, 8>, grid, kWarps * 32, 0, st, a);
+  }
+  return cudaErrorNotSupported;
+}
 
 cudaError_t launch_gemv_small(const GemvArgs& a, int act, int wdt, bool down, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;

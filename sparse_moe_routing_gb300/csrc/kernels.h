@@ -79,7 +79,15 @@ struct GemvArgs {
   // own group (expert ids[p], one token p / k, packed row p), so no
   // bucketing pass is needed; routed_slots = P
   const int32_t* pair_ids;
+  // down + combine in one kernel (pair groups only, see
+  // gemv_small_down_combine_ok): out = r_attn + the combined slots
+  const float* r_attn;      // [T][d]
+  float* out;               // [T][d]
 };
+// Whether the few-token down kernel can also do the combine (pair groups,
+// at most two groups per warp of a column's CTA).
+bool gemv_small_down_combine_ok(const GemvArgs& a);
+cudaError_t launch_gemv_small_down_combine(const GemvArgs& a, int act, int wdt, cudaStream_t st);
 
 // Single-launch decode kernel (decode_fused.cu): the whole layer for a few
 // tokens in one cooperative launch. Route mode (ids_in null): router
