@@ -59,7 +59,8 @@ constexpr int kMaxStages = 4;                  // ring stages per warp, at most
 // the host seeds them with (max, 0) before a call). Marks: 0 start, 1 phase
 // 1 done, 2 past barrier 1, 3 routing rule done, 4 grouping done, 5 phase 3
 // done, 6 past barrier 2, 7 past barrier 3, 8 router tiles done, 9 shared
-// gate/up done, 10 shared-gate row done, 11 down items done.
+// gate/up done, 10 shared-gate row done, 11 down items done, 12 phase-4 h
+// staged.
 #ifdef MOE_DECODE_PHASE_TIMES
 __device__ __forceinline__ void stamp(Ctrl* c, int i) {
   if (threadIdx.x == 0) {
@@ -1327,6 +1328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncthreads();
+      STAMP(12);
       if (!pl4.hs) dn_prime(pl4, f4);
       dn_run(pl4, f4);
       STAMP(11);
