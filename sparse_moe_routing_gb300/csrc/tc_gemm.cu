@@ -210,7 +210,6 @@ constexpr int kEpiWarpBytes = 32 * kEpiRowBytes;
 // 4-bit weights: warps 6 .. 6 + kDequantWarps - 1 dequantise the B stages,
 // one B row (of 256) per thread; warp 6 + kDequantWarps brings the raw codes.
 constexpr int kDequantWarps = 8;
-constexpr int kRowThreads = kDequantWarps / 8;  // threads per B row (256 rows per stage)
 
 // Shared-memory plan of one CTA (1024-byte aligned stages). bf16: kStages
 // stages of A + B, filled by one TMA producer and freed by the MMA. 4-bit:
@@ -308,25 +307,15 @@ __device__ __forceinline__ uint32_t bf16_at(const uint4& v, int j) {
 // e), 128 is subtracted exactly, and one fused multiply-add rounds
 // scale * q + min once.
 __device__ __forceinline__ void dequant_row(const uint8_t* q_row_src, uint8_t* b_stage, int r,
-                                            int part, uint32_t scale_bits, uint32_t min_bits) {
+                                            uint32_t scale_bits, uint32_t min_bits) {
   const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)scale_bits),
                                                 __ushort_as_bfloat16((unsigned short)scale_bits));
   const __nv_bfloat162 m2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)min_bits),
                                                 __ushort_as_bfloat16((unsigned short)min_bits));
   const __nv_bfloat162 b128 = __float2bfloat162_rn(128.0f);
-  // this thread's share of the row: words [c0w, c0w + kW) (16 B of codes per
-  // 32 weights)
-  constexpr int kW = 8 / kRowThreads;
-  const int c0w = part * kW;
-  uint32_t words[kW];
-#pragma unroll
-  for (int h = 0; h < kW / 4; ++h) {
-    const uint4 c = reinterpret_cast<const uint4*>(q_row_src)[c0w / 4 + h];
-    words[4 * h] = c.x;
-    words[4 * h + 1] = c.y;
-    words[4 * h + 2] = c.z;
-    words[4 * h + 3] = c.w;
-  }
+  const uint4 c0 = reinterpret_cast<const uint4*>(q_row_src)[0];
+  const uint4 c1 = reinterpret_cast<const uint4*>(q_row_src)[1];
+  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
   uint8_t* row_base = b_stage + (r >> 3) * 1024 + (r & 7) * 128;
   auto deq = [&](uint32_t pair_bits) {  // (128 + e_lo, 128 + e_hi) -> (w_lo, w_hi)
     __nv_bfloat162 q = *reinterpret_cast<__nv_bfloat162*>(&pair_bits);
@@ -334,11 +323,10 @@ __device__ __forceinline__ void dequant_row(const uint8_t* q_row_src, uint8_t* b
     return *reinterpret_cast<const uint32_t*>(&w);
   };
 #pragma unroll
-  for (int cw = 0; cw < kW; ++cw) {
+  for (int c = 0; c < 8; ++c) {
     // word c holds elements 8c..8c+7, the even element in the low nibble:
     // element e at bits 4e..4e+3
-    const int c = c0w + cw;
-    const uint32_t x = words[cw];
+    const uint32_t x = words[c];
     const uint32_t h04 = deq((x & 0x000F000Fu) | 0x43004300u);          // e0, e4
     const uint32_t h15 = deq(((x >> 4) & 0x000F000Fu) | 0x43004300u);   // e1, e5
     const uint32_t h26 = deq(((x >> 8) & 0x000F000Fu) | 0x43004300u);   // e2, e6
@@ -691,8 +679,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
     // owns B row r. When a row's group count is a multiple of 8, its scales
     // and mins are read 8 groups (16 B) at a time, one block of 8 k-blocks
     // ahead of use.
-    const int r = (threadIdx.x - 192) / kRowThreads;     // B row of this thread
-    const int part = (threadIdx.x - 192) % kRowThreads;  // its share of the row
+    const int r = threadIdx.x - 192;  // B row of this thread
     const bool vec = (a.qgroups & 7) == 0;
     int cs = 0, bs = 0;
     uint32_t cph = 0, bph = 0;
@@ -736,7 +723,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
           alive = false;
           break;
         }
-        dequant_row(sQ + cs * SP::kStageQ + r * 32, sB + bs * kStageB, r, part, sbits, mbits);
+        dequant_row(sQ + cs * SP::kStageQ + r * 32, sB + bs * kStageB, r, sbits, mbits);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
