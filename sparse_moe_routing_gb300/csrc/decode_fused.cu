@@ -4,37 +4,45 @@
 // shared expert, residual) in one kernel, with the expert ids kept on the
 // device as in that page's "NVIDIA CUDA path" (device-routed selected-expert
 // mat-vecs). At a few tokens the layer is a stream of weight rows, and a
-// chain of separate launches spends most of its time between kernels; here
+// chain of separate launches spends much of its time between kernels; here
 // the steps are phases of one cooperative launch (one block per SM)
-// separated by two bounded grid barriers:
+// separated by bounded grid barriers:
 //
 //  1. routing-independent work spread over the grid: router logits
 //     z = W_router x plus the shared-gate logit w_shared . x (column E) and
-//     the shared expert's gate/up + SwiGLU rows; the shared expert's down
-//     rows each block reads in phase 4 are prefetched into L2;
+//     the shared expert's gate/up + SwiGLU rows;
 //  -- grid barrier --
 //  2. every block applies the routing rule to all tokens itself (the router
-//     kernels' own routing code, and logits summed in their order, so ids
-//     and weights equal moe_route's bit for bit), sorts the (token, slot)
-//     pairs by expert into chunks of at most 8 pairs of one expert, and
-//     prefetches into L2 the routed down rows it reads in phase 4; block 0
-//     writes topk_ids and weights;
+//     kernels' own routing code; a routing-only call, moe_route with this
+//     path, runs phases 1-2 of this kernel so that its ids and weights are
+//     the layer's), sorts the (token, slot) pairs by expert into chunks of at
+//     most 8 pairs of one expert; block 0 writes topk_ids and weights;
 //  3. routed gate/up + SwiGLU: (chunk, row) items in a contiguous range per
 //     block; each weight row is read once per chunk and dotted with every
 //     token of the chunk ("Intel SYCL path": one weight load serves all of
 //     an expert's tokens);
 //  -- grid barrier --
-//  4. down x alpha and the combine: block b owns a range of output columns;
-//     items are (4 columns, chunk); the block then sums, per token and
-//     column, its slots in slot order, the shared expert and the residual
-//     (a fixed order: the result is deterministic).
+//  4. down x alpha and the combine, per token and output column: the slots
+//     in slot order, the shared expert and the residual (a fixed order: the
+//     result is deterministic).
+//
+// Two variants. The tensor-core variant (bf16, d a multiple of 1024, I and
+// Is multiples of 128) contracts with mma.sync m16n8k16 on 2D TMA tiles
+// (the tokens are the n = 8 side), splits phase 1 along K when its items
+// would leave half of the grid idle, keeps h in mma fragment order, spreads
+// phase 4 as (8-column group, chunk) items over the whole grid with each
+// block's chunks of h copied to shared memory, and adds a third barrier
+// before the combine. The CUDA-core variant (fp32, or other bf16 shapes)
+// streams rows with 1D bulk copies, owns output columns per block in phase
+// 4 and runs the shared expert's down rows in phase 2 on warps that route no
+// token.
 //
 // Weight bytes reach the SM through one ring of 4 KB stages per warp: each
-// warp copies the next segments of its own work into its ring with
-// cp.async.bulk (lane 0 issues, completion counted by mbarrier transactions)
-// and computes from shared memory, refilling each stage as soon as it has
-// read it. No register holds a load in flight, so every SM keeps its rings
-// (up to 192 KB) of weights in flight.
+// warp copies the next segments of its own work into its ring (lane 0
+// issues, completion counted by mbarrier transactions) and computes from
+// shared memory, refilling each stage as soon as it has read it. No register
+// holds a load in flight, so every SM keeps its rings (up to 192 KB) of
+// weights in flight.
 //
 // Every wait is bounded (about one second; a block that gives up records
 // kDevTimeout in the workspace's status word, lets its copies in flight land
@@ -574,11 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kPairSeg = kSB / 2 / sizeof(TW);       // gate/up elements per stage
   constexpr int kDnSeg = kSB / kDnRows / sizeof(TW);   // down-row elements per stage
 
-  // The shared expert's down rows need only phase 1's results: when some
-  // warps have no token to route, they compute this block's shared-expert
-  // columns while the others route (moved out of phase 4).
-  // (CUDA-core variant; the tensor-core variant keeps them in phase 4,
-  // where they cost no wait on the routing path)
+  // The shared expert's down rows need only phase 1's results: in the
+  // CUDA-core variant, when some warps have no token to route, they compute
+  // this block's shared-expert columns while the others route. The
+  // tensor-core variant keeps them in phase 4, where they hold up no phase.
   const bool sh_early = !MMA && shared && T < kWarps;
   auto down_items = [&](int it0, int it1, int step, int nroute, int nchs) {
     // items (4-column quad qi, chunk ci): ci < nroute a routed chunk, else a
