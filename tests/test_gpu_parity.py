@@ -82,10 +82,18 @@ CASES = [
     (mi.QWEN36_PREFILL_SKEW, 4096, "blocks"),
     (mi.DEEPSEEK_GROUP, 4096, "blocks"),
     (mi.MIXTRAL, 2048, "blocks"),
+    # decode batches of 6-16 tokens take the single-launch kernel: the wide
+    # Mixtral shape (four K segments per warp, h too wide to stage), and
+    # widths that are not powers of two (1408, a 5632-wide shared expert),
+    # 160 experts (router tiles past E)
+    (mi.MIXTRAL, 8, "all"),
     (mi.DEEPSEEK_MOE_64, 1, "all"),
+    (mi.DEEPSEEK_MOE_64, 8, "all"),
     (mi.DEEPSEEK_MOE_64, 256, "blocks"),
     (mi.QWEN_MOE_60, 1, "all"),
     (mi.QWEN_MOE_60, 5, "all"),
+    (mi.QWEN_MOE_60, 12, "all"),
+    (mi.DEEPSEEK_V2_160, 16, "all"),
     (mi.DEEPSEEK_V2_160, 64, "all"),
     (mi.DEEPSEEK_V2_160, 1024, "blocks"),
 ]
@@ -115,6 +123,13 @@ def _check_rows(L, shape, T, dev, mode, seed=0):
 def test_layer_forward_parity(shape, T, mode):
     L, dev, cfg, ws = _run_layer(shape, T)
     _check_rows(L, shape, T, dev, mode)
+
+
+def test_wide_layer_single_launch_forced_at_three_tokens():
+    """The Mixtral-shape layer on the single-launch kernel, forced below the
+    batch size where the automatic choice takes it."""
+    L, dev, cfg, ws = _run_layer(mi.MIXTRAL, 3, smr.PATH_FUSED)
+    _check_rows(L, mi.MIXTRAL, 3, dev, "all")
 
 
 ROUTE_CASES = [(mi.TINY_F32, 32), (mi.QWEN36, 64), (mi.QWEN36_PREFILL_SKEW, 4096),
