@@ -236,18 +236,21 @@ def _cfg(shape, T, path):
         act_dtype=dt[shape.act_dtype], expert_dtype=dt[shape.expert_dtype], path=path)
 
 
-def _fused_mma(shape):
-    """Whether the single-launch kernel's tensor-core variant takes the shape."""
+def _fused_auto(shape):
+    """Whether the library's automatic choice takes the single-launch kernel
+    for this shape (at 6-16 tokens): its tensor-core variant, d_model up to
+    2048 and expert widths up to 1024."""
     return (shape.expert_dtype == "bf16" and shape.act_dtype == "bf16"
             and shape.d_model % 1024 == 0 and shape.d_ff % 128 == 0
-            and shape.d_ff_shared % 128 == 0)
+            and shape.d_ff_shared % 128 == 0 and shape.d_model <= 2048
+            and shape.d_ff <= 1024 and shape.d_ff_shared <= 1024)
 
 
 def _uses_fused(shape, T, path):
     if shape.expert_dtype == "q4" or shape.expert_dtype != shape.act_dtype:
         return False
     if path == 0:  # the library's automatic choice
-        return TC_MIN_TOKENS <= T <= FUSED_MAX_TOKENS and _fused_mma(shape)
+        return TC_MIN_TOKENS <= T <= FUSED_MAX_TOKENS and _fused_auto(shape)
     return path == 3 and T <= FUSED_MAX_TOKENS
 
 

@@ -107,8 +107,9 @@ typedef enum {
   MOE_PATH_AUTO = 0,   /* by shape: CUDA-core GEMV for T <= 5; for T >= 6
                           with bf16 experts the single launch of
                           MOE_PATH_FUSED up to T = 16 when its tensor-core
-                          variant takes the shape (d_model % 1024 == 0,
-                          d_ff and d_ff_shared % 128 == 0), else the
+                          variant takes the shape and it is narrow enough
+                          (d_model 1024 or 2048, d_ff and d_ff_shared
+                          multiples of 128 up to 1024), else the
                           tensor-core grouped GEMM; 4-bit experts always
                           take the tensor-core path. moe_route follows the
                           same choice for its routing kernels. */

@@ -82,10 +82,9 @@ CASES = [
     (mi.QWEN36_PREFILL_SKEW, 4096, "blocks"),
     (mi.DEEPSEEK_GROUP, 4096, "blocks"),
     (mi.MIXTRAL, 2048, "blocks"),
-    # decode batches of 6-16 tokens take the single-launch kernel: the wide
-    # Mixtral shape (four K segments per warp, h too wide to stage), and
-    # widths that are not powers of two (1408, a 5632-wide shared expert),
-    # 160 experts (router tiles past E)
+    # decode batches of 6-16 tokens: the single-launch kernel where it is the
+    # automatic choice (160 experts: router tiles past E), the tensor-core
+    # path on the wider shapes
     (mi.MIXTRAL, 8, "all"),
     (mi.DEEPSEEK_MOE_64, 1, "all"),
     (mi.DEEPSEEK_MOE_64, 8, "all"),
@@ -125,11 +124,18 @@ def test_layer_forward_parity(shape, T, mode):
     _check_rows(L, shape, T, dev, mode)
 
 
-def test_wide_layer_single_launch_forced_at_three_tokens():
-    """The Mixtral-shape layer on the single-launch kernel, forced below the
-    batch size where the automatic choice takes it."""
-    L, dev, cfg, ws = _run_layer(mi.MIXTRAL, 3, smr.PATH_FUSED)
-    _check_rows(L, mi.MIXTRAL, 3, dev, "all")
+# The single-launch kernel forced on the shapes the automatic choice leaves
+# to the tensor-core path: d_model 4096 (four K segments per warp, token
+# fragments loaded per stage), expert widths of 1408 and 14336 and a 5632-wide
+# shared expert (h chunks too wide to stage in shared memory).
+FORCED_FUSED = [(mi.MIXTRAL, 3), (mi.MIXTRAL, 8), (mi.DEEPSEEK_MOE_64, 8), (mi.QWEN_MOE_60, 12)]
+
+
+@pytest.mark.parametrize("shape,T", FORCED_FUSED,
+                         ids=["%s-T%d" % (c[0].name, c[1]) for c in FORCED_FUSED])
+def test_single_launch_forced_on_wide_shapes(shape, T):
+    L, dev, cfg, ws = _run_layer(shape, T, smr.PATH_FUSED)
+    _check_rows(L, shape, T, dev, "all")
 
 
 ROUTE_CASES = [(mi.TINY_F32, 32), (mi.QWEN36, 64), (mi.QWEN36_PREFILL_SKEW, 4096),
