@@ -46,6 +46,7 @@ METRIC = "MoE-layer tokens/s (Qwen3.6 shape, T=1..4096); % of HBM/tensor rooflin
 L2_BYTES = 129 * 10 ** 6
 TC_MIN_TOKENS = 6  # the library's MOE_PATH_AUTO switch away from the GEMV chain
 FUSED_MAX_TOKENS = 16  # the single-launch decode kernel (--path fused) takes up to this many
+FUSED_MIN_TOKENS = 4  # the library's MOE_PATH_AUTO takes it from this many (narrow bf16 shapes)
 
 WORKLOADS = {
     # name: (preset, default T, description)
@@ -238,7 +239,7 @@ def _cfg(shape, T, path):
 
 def _fused_auto(shape):
     """Whether the library's automatic choice takes the single-launch kernel
-    for this shape (at 6-16 tokens): its tensor-core variant, d_model up to
+    for this shape (at 4-16 tokens): its tensor-core variant, d_model up to
     2048 and expert widths up to 1024."""
     return (shape.expert_dtype == "bf16" and shape.act_dtype == "bf16"
             and shape.d_model % 1024 == 0 and shape.d_ff % 128 == 0
@@ -250,7 +251,7 @@ def _uses_fused(shape, T, path):
     if shape.expert_dtype == "q4" or shape.expert_dtype != shape.act_dtype:
         return False
     if path == 0:  # the library's automatic choice
-        return TC_MIN_TOKENS <= T <= FUSED_MAX_TOKENS and _fused_auto(shape)
+        return FUSED_MIN_TOKENS <= T <= FUSED_MAX_TOKENS and _fused_auto(shape)
     return path == 3 and T <= FUSED_MAX_TOKENS
 
 

@@ -104,15 +104,15 @@ typedef enum {
 
 /* Expert-path selection for moe_layer_forward / moe_experts_forward. */
 typedef enum {
-  MOE_PATH_AUTO = 0,   /* by shape: CUDA-core GEMV for T <= 5; for T >= 6
-                          with bf16 experts the single launch of
-                          MOE_PATH_FUSED up to T = 16 when its tensor-core
+  MOE_PATH_AUTO = 0,   /* by shape: with bf16 experts the single launch of
+                          MOE_PATH_FUSED for 4 <= T <= 16 when its tensor-core
                           variant takes the shape and it is narrow enough
                           (d_model 1024 or 2048, d_ff and d_ff_shared
-                          multiples of 128 up to 1024), else the
-                          tensor-core grouped GEMM; 4-bit experts always
-                          take the tensor-core path. moe_route follows the
-                          same choice for its routing kernels. */
+                          multiples of 128 up to 1024); otherwise CUDA-core
+                          GEMV for T <= 5 and the tensor-core grouped GEMM
+                          for T >= 6; 4-bit experts always take the
+                          tensor-core path. moe_route follows the same
+                          choice for its routing kernels. */
   MOE_PATH_GEMV = 1,   /* CUDA-core weight-streaming GEMV at any T */
   MOE_PATH_TC = 2,     /* tcgen05 grouped GEMM: bf16 or 4-bit experts with bf16
                           activations, d_model % 256 == 0, d_ff % 128 == 0,

@@ -57,23 +57,26 @@ int tc_router_bn(const moe_cfg_t& c) {
 }
 
 // The single-launch decode kernel runs when asked for (MOE_PATH_FUSED), and
-// is MOE_PATH_AUTO's choice for kTcMinTokens..kDecodeMaxTokens tokens when
-// its tensor-core variant takes the shape (bf16) and the shape is one where
-// it was measured faster: d_model <= 2048 (each warp keeps its token
+// is MOE_PATH_AUTO's choice for kFusedMinTokens..kDecodeMaxTokens tokens
+// when its tensor-core variant takes the shape (bf16) and the shape is one
+// where it was measured faster: d_model <= 2048 (each warp keeps its token
 // fragments in registers) and expert widths <= 1024 (a block's chunks of h
-// fit shared memory). Per layer (single launch / tensor-core path / GEMV
-// chain): Qwen3.6 shape T=1 31 / - / 22 us, T=2 43 / - / 35 us, T=4 57 / - /
-// 58 us, T=8 80 / 93 / - us, T=12 115 / 125 / - us, T=16 133 / 143 / - us;
-// sigmoid-group shape T=8 76 / 90 us, T=16 106 / 113 us; but the
-// Mixtral shape (d_model 4096, width 14336) T=8 545 / 398 us. Below
-// kTcMinTokens the GEMV chain stays: its launches cost less than the
-// kernel's three grid barriers and in-kernel routing.
+// fit shared memory). Per layer (single launch / GEMV chain / tensor-core
+// path): Qwen3.6 shape T=1 31 / 21 / - us, T=2 43 / 35 / - us, T=3 51 / 47 /
+// - us, T=4 57 / 56 / - us, T=5 67 / 84 / - us, T=6 70 / 97 / - us, T=8
+// 80 / - / 93 us, T=12 115 / - / 125 us, T=16 133 / - / 143 us;
+// sigmoid-group shape T=4 57 / 61 us, T=5 60 / 87 us, T=8 76 / - / 90 us,
+// T=16 106 / - / 113 us; but the Mixtral shape (d_model 4096, width 14336)
+// T=8 545 / - / 398 us. Below kFusedMinTokens the GEMV chain stays: its
+// launches cost less than the kernel's three grid barriers and in-kernel
+// routing.
+constexpr int kFusedMinTokens = 4;
 bool fused_ok(const moe_cfg_t& c) {
   return decode_fused_supported(c.T, c.d_model, c.n_experts, c.top_k, c.d_ff, c.d_ff_shared,
                                 c.act_dtype, c.expert_dtype);
 }
 bool auto_fused(const moe_cfg_t& c) {
-  return c.path == MOE_PATH_AUTO && c.T >= kTcMinTokens && c.T <= kDecodeMaxTokens &&
+  return c.path == MOE_PATH_AUTO && c.T >= kFusedMinTokens && c.T <= kDecodeMaxTokens &&
          c.act_dtype == MOE_BF16 && c.expert_dtype == MOE_BF16 && c.d_model <= 2048 &&
          c.d_ff <= 1024 && c.d_ff_shared <= 1024 &&
          decode_fused_mma(c.d_model, c.d_ff, c.d_ff_shared) && fused_ok(c);
