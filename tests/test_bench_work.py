@@ -62,3 +62,20 @@ def test_gateup_launch_unit():
     assert b == 224 * 4_194_304 + 64 * 2048 * 2
     # 2 x 2048 x 1024 per routed pair (512 pairs) and per shared row (64)
     assert f == (512 + 64) * 2 * 2048 * 1024
+
+
+def test_expert_path_labels_follow_the_automatic_choice():
+    # MOE_PATH_AUTO (path 0): GEMV chain up to 3 tokens, the single launch for
+    # 4-16 tokens on the narrow bf16 shapes (d_model <= 2048, widths <= 1024),
+    # the tensor-core path above 16 tokens and on the wider shapes from 6
+    auto = 0
+    assert bench._expert_path(QWEN, 3, auto) == "CUDA-core direct-load GEMV"
+    for T in (4, 8, 16):
+        assert bench._expert_path(QWEN, T, auto) == "single-launch decode kernel"
+    assert bench._expert_path(QWEN, 17, auto) == "tcgen05 grouped GEMM"
+    assert bench._expert_path(MIX, 5, auto) == "CUDA-core direct-load GEMV"
+    assert bench._expert_path(MIX, 8, auto) == "tcgen05 grouped GEMM"
+    assert bench._expert_path(MIX_Q4, 8, auto) == "tcgen05 grouped GEMM"
+    # forced single launch (path 3) up to 16 tokens, on any shape
+    assert bench._expert_path(MIX, 3, 3) == "single-launch decode kernel"
+    assert bench._expert_path(QWEN, 17, 3) != "single-launch decode kernel"
