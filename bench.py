@@ -5,10 +5,12 @@ Default workload: the Qwen3.6-35B-A3B MoE layer shape (d_model 2048, 256
 routed experts, top-8 softmax with renormalisation, expert and shared
 intermediate 512, one sigmoid-gated shared expert), synthetic seeded weights
 N(0, 0.02) in bf16 and RMS-normalised activations, at the decode batch T=64
-(the sweep also runs T = 1 and 8). One step = one full layer forward (router,
-routing rule, bucketing, routed experts, shared expert, combine, residual).
-Other workloads (--workload prefill | deepseek | mixtral) run the other
-shapes of the same family for measurement; the default is the headline.
+(the sweep also runs T = 1 and 8, prefill, the sigmoid-group layer and the
+Mixtral-shape layers). One step = one full layer forward (router, routing
+rule, bucketing, routed experts, shared expert, combine, residual). Other
+workloads (--workload prefill | deepseek | mixtral | mixtral_q4 |
+deepseek_moe_64 | qwen_moe_60 | deepseek_v2_160) run the other shapes for
+measurement; the default is the headline.
 
 Timing: K steps are captured into one CUDA graph and replayed (W eager
 warm-up steps first). Consecutive steps use distinct copies of the layer's
@@ -19,7 +21,7 @@ bracketed by events inside the graph (moe_trace_kernel) in a second replay, so
 the event nodes do not add to the timed step.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--tokens T]
-                       [--workload decode|prefill|deepseek|mixtral]
+                       [--workload decode|prefill|deepseek|mixtral|mixtral_q4|...]
                        [--path auto|gemv|tc|fused] [--impl ours|reference]
                        [--no-sweep] [--no-cpu-baseline] [--no-hot-l2] [--breakdown]
 For N > 1 launch with torchrun (one rank per GPU, NCCL): every rank runs an
@@ -57,6 +59,14 @@ WORKLOADS = {
     "mixtral": ("mixtral_bf16", 2048, "mixtral-style top-2 layer, bf16, T=%d"),
     "mixtral_q4": ("mixtral_q4", 2048,
                    "mixtral-style top-2 layer, 4-bit affine g64 experts, T=%d"),
+    # further expert counts (experts / top-k of the Airframe model table; the
+    # widths are the generator's choice), not part of the default sweep
+    "deepseek_moe_64": ("deepseek_moe_64", 256,
+                        "64-expert top-6 layer with a shared expert, width 1408, T=%d"),
+    "qwen_moe_60": ("qwen_moe_60", 64,
+                    "60-expert top-4 layer with a 5632-wide shared expert, width 1408, T=%d"),
+    "deepseek_v2_160": ("deepseek_v2_160", 1024,
+                        "160-expert top-6 layer with a shared expert, width 512, T=%d"),
 }
 
 
@@ -255,10 +265,23 @@ def _uses_fused(shape, T, path):
     return path == 3 and T <= FUSED_MAX_TOKENS
 
 
+def _tc_shape(shape):
+    """The library's tensor-core path shapes: bf16 activations, d_model a
+    multiple of 256, widths of 128, a shared expert absent or as wide as the
+    routed ones (absent for 4-bit banks)."""
+    if shape.act_dtype != "bf16" or shape.d_model % 256 or shape.d_ff % 128:
+        return False
+    if shape.expert_dtype == "q4":
+        return shape.d_ff_shared == 0
+    return shape.expert_dtype == "bf16" and shape.d_ff_shared in (0, shape.d_ff)
+
+
 def _uses_tc(shape, T, path):
+    if not _tc_shape(shape):
+        return False
     if shape.expert_dtype == "q4":
         return True  # 4-bit banks are dequantised inside the tensor-core kernel
-    if shape.expert_dtype != "bf16" or _uses_fused(shape, T, path):
+    if _uses_fused(shape, T, path):
         return False
     return path == 2 or (path == 0 and T >= TC_MIN_TOKENS)
 

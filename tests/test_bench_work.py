@@ -79,3 +79,11 @@ def test_expert_path_labels_follow_the_automatic_choice():
     # forced single launch (path 3) up to 16 tokens, on any shape
     assert bench._expert_path(MIX, 3, 3) == "single-launch decode kernel"
     assert bench._expert_path(QWEN, 17, 3) != "single-launch decode kernel"
+
+
+def test_expert_path_label_of_a_shape_the_tensor_cores_do_not_take():
+    # a shared expert wider than the routed ones (5632 against 1408) keeps the
+    # layer on the CUDA-core GEMV kernels at every batch size
+    q60 = mi.PRESETS["qwen_moe_60"]
+    assert bench._expert_path(q60, 64, 0) == "CUDA-core streaming GEMV"
+    assert bench._expert_path(q60, 5, 0) == "CUDA-core direct-load GEMV"
