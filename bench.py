@@ -267,13 +267,13 @@ def _uses_fused(shape, T, path):
 
 def _tc_shape(shape):
     """The library's tensor-core path shapes: bf16 activations, d_model a
-    multiple of 256, widths of 128, a shared expert absent or as wide as the
-    routed ones (absent for 4-bit banks)."""
+    multiple of 256, widths multiples of 128 (no shared expert for 4-bit
+    banks)."""
     if shape.act_dtype != "bf16" or shape.d_model % 256 or shape.d_ff % 128:
         return False
     if shape.expert_dtype == "q4":
         return shape.d_ff_shared == 0
-    return shape.expert_dtype == "bf16" and shape.d_ff_shared in (0, shape.d_ff)
+    return shape.expert_dtype == "bf16" and shape.d_ff_shared % 128 == 0
 
 
 def _uses_tc(shape, T, path):
@@ -338,17 +338,25 @@ def _n_copies(shape, T):
     return int(min(16, max(2, math.ceil(4 * L2_BYTES / touched) + 1)))
 
 
+class StepDurations(list):
+    """Per-step durations (ms) of one traced kernel family: the sum of the
+    family's launches within each step (`per` launches per step)."""
+    per = 1
+
+
 def time_graph(wl, K, W, trace_kernel=None, sampler=None, extra_replays=0):
     """Eager warm-up, then one CUDA graph of K steps replayed once (timed);
     extra_replays more timed replays after it (their ms in the last slot of
-    the result)."""
+    the result). With trace_kernel, the third slot holds that family's
+    duration per step (StepDurations: a family may launch more than once per
+    step, e.g. a shared expert of another width has its own launches)."""
     import torch
     import sparse_moe_routing_gb300 as smr
     for i in range(W):
         wl.step(i)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
-    tr = smr.KernelTrace(trace_kernel, K) if trace_kernel else None
+    tr = smr.KernelTrace(trace_kernel, 4 * K) if trace_kernel else None
     n0 = smr.launch_count()
     if tr:
         tr.__enter__()
@@ -383,7 +391,12 @@ def time_graph(wl, K, W, trace_kernel=None, sampler=None, extra_replays=0):
         time.sleep(0.1)
         sampler.stop()
     ms = s.elapsed_time(e)
-    durs = tr.durations_ms() if tr else []
+    durs = StepDurations()
+    if tr:
+        per = max(1, tr.count // K)
+        one = tr.durations_ms()
+        durs.per = per
+        durs.extend(sum(one[i * per:(i + 1) * per]) for i in range(len(one) // per))
     extra = []
     for _ in range(extra_replays):
         s.record()
@@ -694,7 +707,11 @@ def run_ours(args):
                 "algorithmic_flops_per_launch": gf,
                 "units_per_launch": (1 if kern == "decode_fused" else
                                      n_act + (1 if shape.d_ff_shared else 0)),
-                "mean_launch_us": mean_k * 1e3 if mean_k else None}
+                "mean_launch_us": mean_k * 1e3 if mean_k else None,
+                # launches of the family per step (2 when a shared expert of
+                # another width has its own launch): the figures above are
+                # per step, all of them together
+                "launches_per_step": getattr(durs, "per", 1)}
     lb, lf = layer_bytes(shape, T, n_act), layer_flops(shape, T)
     config = dict(workload_config(shape, T, desc))
     config.update({

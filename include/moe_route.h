@@ -116,9 +116,12 @@ typedef enum {
   MOE_PATH_GEMV = 1,   /* CUDA-core weight-streaming GEMV at any T */
   MOE_PATH_TC = 2,     /* tcgen05 grouped GEMM: bf16 or 4-bit experts with bf16
                           activations, d_model % 256 == 0, d_ff % 128 == 0,
-                          d_ff_shared 0 or == d_ff (4-bit: 0); other shapes
-                          return MOE_ERR_UNSUPPORTED (and MOE_PATH_AUTO then
-                          uses the GEMV path) */
+                          d_ff_shared % 128 == 0 (a shared expert as wide as
+                          the routed ones is one more group of their GEMMs,
+                          one of another width runs as its own launches;
+                          4-bit: no shared expert); other shapes return
+                          MOE_ERR_UNSUPPORTED (and MOE_PATH_AUTO then uses
+                          the GEMV path) */
   MOE_PATH_FUSED = 3   /* one cooperative launch (one block per SM) for the
                           whole layer, the device-routed decode of the
                           Treebeard page's "NVIDIA CUDA path": routing,

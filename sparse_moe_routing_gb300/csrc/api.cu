@@ -38,7 +38,13 @@ constexpr int kTcMinTokens = 6;
 bool tc_shape_ok(const moe_cfg_t& c) {
   if (c.act_dtype != MOE_BF16 || c.d_model % 256 != 0 || c.d_ff % 128 != 0) return false;
   if (c.expert_dtype == MOE_Q4_AFFINE_G64) return c.d_ff_shared == 0;
-  return c.expert_dtype == MOE_BF16 && (c.d_ff_shared == 0 || c.d_ff_shared == c.d_ff);
+  return c.expert_dtype == MOE_BF16 && c.d_ff_shared % 128 == 0;
+}
+// A shared expert of another width than the routed ones cannot be one more
+// group of their grouped GEMMs (other N tiling, and another K for down): it
+// runs as its own gate/up and down launches of the same kernels.
+bool shared_apart(const moe_cfg_t& c) {
+  return c.d_ff_shared > 0 && c.d_ff_shared != c.d_ff;
 }
 
 // The router contraction on the tensor cores: bf16, E a multiple of 32 (N
@@ -400,7 +406,7 @@ BucketArgs bucket_args(const int32_t* ids, const moe_cfg_t* c, int32_t* counts,
     b.rowblocks = at<int2>(c, p.rowblocks);
     b.n_rowblocks = &at<Ctrl>(c, 0)->n_rowblocks;
     b.bm = kTcBm;
-    b.shared_rows = c->d_ff_shared > 0 ? c->T : 0;
+    b.shared_rows = (c->d_ff_shared > 0 && !shared_apart(*c)) ? c->T : 0;
     b.pair = use_pair(*c) ? 1 : 0;
   }
   return b;
@@ -441,7 +447,8 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
   Ctrl* ctrl = at<Ctrl>(c, 0);
   const int T = c->T, d = c->d_model, E = c->n_experts, k = c->top_k, I = c->d_ff;
   const int Is = c->d_ff_shared, P = T * k;
-  const bool shared = Is > 0;
+  const bool apart = shared_apart(*c);
+  const bool shared = Is > 0 && !apart;  // the shared expert is a group of the routed launches
   void* xperm = at<void>(c, p.Xperm);
   void* H = at<void>(c, p.H);
   void* Hs = at<void>(c, p.Hs);
@@ -512,6 +519,26 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
   e = run(MOE_KERNEL_TC_GATEUP, st,
           [&] { return launch_tc_gemm(kTcGateUp, m, a, max_rb * a.n_tiles, st); });
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const int shared_rb = (T + kTcBm - 1) / kTcBm;
+  if (apart) {
+    // the shared expert alone: A = x, B = its gate and up rows, out Hs [T][Is]
+    TcMaps ms{};
+    if (!tc_make_map(&ms.A1, x, T, d, arows) || !tc_make_map(&ms.B2, Wsg, Is, d, gu_rows) ||
+        !tc_make_map(&ms.B3, Wsu, Is, d, gu_rows))
+      return MOE_ERR_CUDA;
+    ms.A0 = ms.A1;
+    ms.B0 = ms.B2;
+    ms.B1 = ms.B3;
+    TcArgs as = a;
+    as.shared_only = 1;
+    as.pair = 0;
+    as.ld_out = Is;
+    as.n_tiles = Is / gu_rows;
+    as.wait_ns = take_stall(MOE_KERNEL_TC_GATEUP, &as.stall);
+    e = run(MOE_KERNEL_TC_GATEUP, st,
+            [&] { return launch_tc_gemm(kTcGateUp, ms, as, shared_rb * as.n_tiles, st); });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
 
   // down: A = H (routed) / Hs (shared), B = down rows; alpha in the epilogue
   TcMaps m2{};
@@ -542,9 +569,26 @@ moe_status_t enqueue_experts_tc(const void* x, const float* r_attn, const float*
   e = run(MOE_KERNEL_TC_DOWN, st,
           [&] { return launch_tc_gemm(kTcDown, m2, a, max_rb * a.n_tiles, st); });
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (apart) {
+    // the shared expert's down alone: A = Hs, B = its down rows, out Ys x s_t
+    TcMaps ms{};
+    if (!tc_make_map(&ms.A1, Hs, T, Is, arows) || !tc_make_map(&ms.B2, Wsd, d, Is, 256))
+      return MOE_ERR_CUDA;
+    ms.A0 = ms.A1;
+    ms.B0 = ms.B1 = ms.B3 = ms.B2;
+    TcArgs as = a;
+    as.shared_only = 1;
+    as.pair = 0;
+    as.K = Is;
+    as.qs0 = as.qm0 = nullptr;
+    as.wait_ns = take_stall(MOE_KERNEL_TC_DOWN, &as.stall);
+    e = run(MOE_KERNEL_TC_DOWN, st,
+            [&] { return launch_tc_gemm(kTcDown, ms, as, shared_rb * as.n_tiles, st); });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
 
   CombineArgs cb{r_attn, static_cast<const float*>(Y),
-                 shared ? static_cast<const float*>(Ys) : nullptr, at<int32_t>(c, p.pos), out,
+                 Is > 0 ? static_cast<const float*>(Ys) : nullptr, at<int32_t>(c, p.pos), out,
                  T, d, k, 1};
   return cuda_status(run(MOE_KERNEL_COMBINE, st, [&] { return launch_combine(cb, st); }));
 }

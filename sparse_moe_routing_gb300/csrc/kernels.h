@@ -171,6 +171,9 @@ struct TcArgs {
   // the B tiles (the bucketing pass then lists every second block); 4-bit
   // banks only
   int pair;
+  // 1: the launch's items are the shared expert's alone (row blocks of the T
+  // token rows, no row-block list), for a shared expert of another width
+  int shared_only;
   // box height of the A maps (gate/up and down, bf16): 128, or 64 / 16 when
   // every group holds at most that many rows
   int arows;

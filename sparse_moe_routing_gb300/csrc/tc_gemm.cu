@@ -179,6 +179,12 @@ __device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, int t, int n_rb
     ti.row0 = 0;
     ti.rows = a.T;
     ti.shared = false;
+  } else if (a.shared_only) {
+    ti.g = a.E;
+    ti.m = rb;
+    ti.row0 = 0;
+    ti.rows = a.T;
+    ti.shared = true;
   } else {
     const int2 r = a.rowblocks[rb];
     ti.g = r.x;
@@ -402,7 +408,7 @@ __global__ void __launch_bounds__(SmemPlan<Q4, RB, MODE == kTcDown, NB, AR>::kTh
   pdl_wait();
   pdl_trigger();
 
-  const int n_rb = MODE == kTcRouter ? (a.T + BM - 1) / BM : *a.n_rowblocks;
+  const int n_rb = (MODE == kTcRouter || a.shared_only) ? (a.T + BM - 1) / BM : *a.n_rowblocks;
   const int total = n_rb * a.n_tiles;
   const int nkb = a.K / BK;
 

@@ -81,9 +81,12 @@ def test_expert_path_labels_follow_the_automatic_choice():
     assert bench._expert_path(QWEN, 17, 3) != "single-launch decode kernel"
 
 
-def test_expert_path_label_of_a_shape_the_tensor_cores_do_not_take():
-    # a shared expert wider than the routed ones (5632 against 1408) keeps the
-    # layer on the CUDA-core GEMV kernels at every batch size
+def test_expert_path_labels_of_other_shapes():
+    # a shared expert wider than the routed ones (5632 against 1408) runs as
+    # its own tensor-core launches; widths above 1024 leave the single launch
     q60 = mi.PRESETS["qwen_moe_60"]
-    assert bench._expert_path(q60, 64, 0) == "CUDA-core streaming GEMV"
+    assert bench._expert_path(q60, 64, 0) == "tcgen05 grouped GEMM"
+    assert bench._expert_path(q60, 8, 0) == "tcgen05 grouped GEMM"
     assert bench._expert_path(q60, 5, 0) == "CUDA-core direct-load GEMV"
+    tiny = mi.PRESETS["tiny_f32"]
+    assert bench._expert_path(tiny, 32, 0) == "CUDA-core streaming GEMV"

@@ -92,6 +92,8 @@ CASES = [
     (mi.QWEN_MOE_60, 1, "all"),
     (mi.QWEN_MOE_60, 5, "all"),
     (mi.QWEN_MOE_60, 12, "all"),
+    (mi.QWEN_MOE_60, 64, "all"),
+    (mi.QWEN_MOE_60, 300, "blocks"),
     (mi.DEEPSEEK_V2_160, 16, "all"),
     (mi.DEEPSEEK_V2_160, 64, "all"),
     (mi.DEEPSEEK_V2_160, 1024, "blocks"),
