@@ -73,7 +73,9 @@ int tc_router_bn(const moe_cfg_t& c) {
 // 80 / - / 93 us, T=12 115 / - / 125 us, T=16 133 / - / 143 us;
 // sigmoid-group shape T=4 57 / 61 us, T=5 60 / 87 us, T=8 76 / - / 90 us,
 // T=16 106 / - / 113 us; but the Mixtral shape (d_model 4096, width 14336)
-// T=8 545 / - / 398 us. Below kFusedMinTokens the GEMV chain stays: its
+// T=8 545 / - / 398 us, and at width 1408 T=8 135 / - / 128 us (64 experts)
+// and 284 / - / 163 us (60 experts, 5632-wide shared expert). Below
+// kFusedMinTokens the GEMV chain stays: its
 // launches cost less than the kernel's three grid barriers and in-kernel
 // routing.
 constexpr int kFusedMinTokens = 4;
